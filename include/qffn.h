@@ -1,0 +1,200 @@
+/*
+ * qffn -- FP8-quantised SwiGLU feed-forward block for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every entry point takes plain pointers and sizes and returns a
+ * qffn_status; nothing here allocates device memory, and every buffer is
+ * owned by the caller.
+ *
+ * Sources of the operations (page title, function):
+ *   [llmq-model]  IST-DASLab/llmq "src/models/llama_model.cpp":
+ *                 LLamaModel::_forward_block (FFN half), forward_qmm,
+ *                 _recompute_block (swiglu_forward_quant), fill_block_shapes,
+ *                 LLamaModel::forward (fill_zero of the abs-max block).
+ *   [llmq-state]  IST-DASLab/llmq "src/models/llama_run_state.cpp":
+ *                 activation shapes and dtypes, the stats block (two floats per
+ *                 quantised tensor: abs-max, then scale).
+ *   [metrale]     metrale "layers/dense_ffn_decode.rs", DenseFfnLayer::forward,
+ *                 FP8 arm: w8a16_gemv_dual, silu_mul, w8a16_gemv.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensors are row-major and contiguous.  uint16_t* holds bf16 bit patterns,
+ *    uint8_t* holds OCP FP8 E4M3 ("fn") codes, float* is IEEE binary32.
+ *  - "stats" points at two device floats {abs_max, scale} [llmq-state].  A
+ *    call that records an abs-max first zeroes stats[0] on the stream (the
+ *    trainer's fill_zero before the forward) and then max-accumulates into it.
+ *  - scale = abs_max / 448 is the dequantisation multiplier (448 = largest
+ *    finite E4M3); codes are e4m3(x * (448 / abs_max)) with the product in
+ *    fp32, rounded to nearest even and saturated to +-448.  abs_max == 0 gives
+ *    scale 1 and all-zero codes.
+ *  - Device pointers must be 16-byte aligned (QFFN_ERR_MISALIGNED otherwise);
+ *    required pointers must be non-NULL (QFFN_ERR_INVALID_ARG).
+ *  - Arguments are checked on the host before anything is enqueued; on any
+ *    error nothing is enqueued.  Work is enqueued asynchronously on `stream`
+ *    (NULL = the legacy default stream) and the call returns without waiting.
+ *    Launch failures are reported as QFFN_ERR_CUDA.
+ *  - The GEMM kernels bound every wait on their internal pipeline barriers.
+ *    A wait that runs out (about 2 s) makes the kernel stop, set a device
+ *    status word and return; qffn_check_status() reports it.
+ *  - Output buffers must not overlap inputs unless a call says otherwise.
+ */
+#ifndef QFFN_H_
+#define QFFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* qffn_stream_t;
+
+typedef enum qffn_status {
+  QFFN_OK = 0,
+  QFFN_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, bad eps, small workspace */
+  QFFN_ERR_UNSUPPORTED_SHAPE = 2, /* a size outside the rules stated per call */
+  QFFN_ERR_MISALIGNED = 3,        /* a pointer not 16-byte aligned */
+  QFFN_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+  QFFN_ERR_TIMEOUT = 5            /* a device-side bounded wait ran out */
+} qffn_status;
+
+/* Static description of a status code. */
+const char* qffn_status_string(qffn_status status);
+
+/* Version of this ABI (bumped on any signature change). */
+int qffn_abi_version(void);
+
+/* Synchronises `stream`, then reports (and clears) the device status word:
+ * QFFN_ERR_TIMEOUT if a GEMM kernel gave up on a pipeline wait since the last
+ * check, QFFN_ERR_CUDA if the synchronisation failed, else QFFN_OK. */
+qffn_status qffn_check_status(qffn_stream_t stream);
+
+/* ---- Step A1: fused residual add + RMSNorm + abs-max -----------------------
+ * [llmq-model] fused_residual_rmsnorm_forward (and rmsnorm_forward when
+ * res_in == NULL), called in _forward_block before the up projection.
+ *   res_out[N,C] = bf16(res_in + x)                        (skipped if res_in == NULL)
+ *   rstd[N]      = 1 / sqrt(mean_C(r^2) + eps),  r = res_out (or x)
+ *   y[N,C]       = bf16(r * rstd * gain)
+ *   stats[0]     = max |y|   (zeroed first; stats == NULL records nothing)
+ * res_out may alias res_in or x (in place).  N >= 0, C % 8 == 0,
+ * 8 <= C <= 16384; eps >= 0 and finite. */
+qffn_status qffn_rmsnorm_absmax(uint16_t* res_out, uint16_t* y, float* rstd, float* stats,
+                                const uint16_t* res_in, const uint16_t* x, const uint16_t* gain,
+                                float eps, int64_t N, int64_t C, qffn_stream_t stream);
+
+/* ---- Tensor abs-max -------------------------------------------------------
+ * [llmq-model] abs_max: stats[0] = max |in[i]| over n bf16 values (zeroed
+ * first).  Used to build per-tensor FP8 weight records.  n >= 0. */
+qffn_status qffn_absmax(float* stats, const uint16_t* in, int64_t n, qffn_stream_t stream);
+
+/* ---- Step A2: quantise with a recorded abs-max -----------------------------
+ * [llmq-model] forward_qmm -> quantize_with_abs_max.  Reads stats[0]
+ * (abs_max, produced earlier on the stream), writes stats[1] = scale and
+ * q[i] = e4m3(in[i] * 448 / abs_max).  n >= 0. */
+qffn_status qffn_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t n,
+                          qffn_stream_t stream);
+
+/* ---- Per-row FP8 weight record (decode weights) ---------------------------
+ * [metrale] fp8 weights carry a per-output-row fp32 row_scale.  For each row:
+ * row_scale[r] = max_k |w[r,k]| / 448, q[r,k] = e4m3(w[r,k] * 448 / rowmax)
+ * (a zero row gives scale 1, codes 0).  rows >= 0, cols % 16 == 0,
+ * 16 <= cols <= 65536. */
+qffn_status qffn_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, int64_t rows,
+                               int64_t cols, qffn_stream_t stream);
+
+/* ---- Steps A3 / A5: scaled FP8 GEMM ---------------------------------------
+ * [llmq-model] forward_qmm -> matmul(out, W, X, bias=none, scale_W, scale_X,
+ * OC, B*T, C, TN): both operands FP8 with K contiguous, bf16 output.
+ *   out[M,N] = bf16(a_scale[0] * w_scale[0] * sum_k A[m,k] * W[n,k])
+ * fp32 accumulation on the tensor cores.  a_scale / w_scale are device
+ * pointers to one float each.  M >= 0, N % 32 == 0, K % 16 == 0, K >= 16,
+ * N, K <= 2^20. */
+qffn_status qffn_fp8_gemm_scaled(uint16_t* out, const uint8_t* A, const float* a_scale,
+                                 const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
+                                 int64_t K, qffn_stream_t stream);
+
+/* ---- Steps A3 + A4 fused: gate|up GEMM with the SwiGLU epilogue -----------
+ * [llmq-model] forward_qmm on MLP_Up_w (W1 = [2H, C], gate rows [0,H) then up
+ * rows [H,2H)) followed by swiglu_forward with its abs-max.  The gate and up
+ * products are each rounded to bf16 (the mlp_up buffer dtype) before
+ *   h[N,H]      = bf16(silu(g) * u),  silu(z) = z / (1 + exp(-z))
+ *   stats_h[0]  = max |h|   (zeroed first)
+ * The [N, 2H] up-projection output is never written.  N >= 0,
+ * C % 16 == 0, C >= 16, H % 128 == 0, H >= 128, C, H <= 2^20. */
+qffn_status qffn_gate_up_swiglu(uint16_t* h, float* stats_h, const uint8_t* yq,
+                                const float* y_scale, const uint8_t* w1, const float* w1_scale,
+                                int64_t N, int64_t C, int64_t H, qffn_stream_t stream);
+
+/* ---- Step A4 standalone: SwiGLU + abs-max + requantisation ----------------
+ * [llmq-model] swiglu_forward then quantize_with_abs_max; the h == NULL form
+ * is swiglu_forward_quant of _recompute_block (h recomputed for the second
+ * pass, bit-identical).  gate_up is [N, 2H] bf16 (gate = cols [0,H)).
+ *   h[N,H] = bf16(silu(g) * u); stats[0] = max|h|; stats[1] = scale;
+ *   hq[N,H] = e4m3(h * 448 / max|h|).   N >= 0, H % 8 == 0. */
+qffn_status qffn_swiglu_quant(uint16_t* h, uint8_t* hq, float* stats, const uint16_t* gate_up,
+                              int64_t N, int64_t H, qffn_stream_t stream);
+
+/* ---- Whole prefill FFN: A1 -> A2 -> A3+A4 -> A2 -> A5 ---------------------
+ * [llmq-model] _forward_block, FFN half, for B*T tokens:
+ *   r = bf16(res_in + x); y = rmsnorm(r) * gain; yq = quant(y);
+ *   h = swiglu(yq @ W1^T); hq = quant(h); out = bf16(hq @ W2^T * scales)
+ * Outputs: res_out [N,C] (the residual the next layer adds `out` to), out
+ * [N,C] bf16, rstd [N] fp32, stats_y[2], stats_h[2].  w1 = [2H, C] E4M3 with
+ * per-tensor scale w1_scale[1]; w2 = [C, H] E4M3 with w2_scale[1] (device).
+ * res_in == NULL runs the plain RMSNorm (res_out unused, may be NULL).
+ * workspace: device scratch of at least qffn_forward_workspace_size() bytes,
+ * 256-byte aligned, holding y, yq, h, hq at the offsets that
+ * qffn_forward_workspace_offsets() returns (readable after the call).
+ * N = B*T >= 0, C % 128 == 0, H % 128 == 0, 128 <= C <= 16384,
+ * 128 <= H <= 2^20. */
+size_t qffn_forward_workspace_size(int64_t B, int64_t T, int64_t C, int64_t H);
+qffn_status qffn_forward_workspace_offsets(int64_t B, int64_t T, int64_t C, int64_t H,
+                                           size_t offsets[4] /* y, yq, h, hq */);
+qffn_status qffn_forward(uint16_t* res_out, uint16_t* out, float* rstd, float* stats_y,
+                         float* stats_h, const uint16_t* res_in, const uint16_t* x,
+                         const uint16_t* gain, float eps, const uint8_t* w1,
+                         const float* w1_scale, const uint8_t* w2, const float* w2_scale,
+                         int64_t B, int64_t T, int64_t C, int64_t H, void* workspace,
+                         size_t workspace_bytes, qffn_stream_t stream);
+
+/* ---- Step A6: dual row-scaled FP8 GEMV ------------------------------------
+ * [metrale] w8a16_gemv_dual: one pass over x for two weight matrices.
+ *   g[r] = bf16(s_gate[r] * sum_k Wg[r,k] * x[k]),  u likewise with Wu, s_up.
+ * Wg, Wu are [H, C] E4M3; s_gate, s_up [H] fp32; x [C] bf16; g, u [H] bf16.
+ * C % 16 == 0, 16 <= C <= 32768, H >= 1. */
+qffn_status qffn_gemv_dual(uint16_t* g, uint16_t* u, const uint16_t* x, const uint8_t* w_gate,
+                           const float* s_gate, const uint8_t* w_up, const float* s_up,
+                           int64_t H, int64_t C, qffn_stream_t stream);
+
+/* ---- Row-scaled FP8 GEMV (steps A6 per projection, A8) --------------------
+ * [metrale] w8a16_gemv: out[r] = bf16(row_scale[r] * sum_k W[r,k] * x[k]).
+ * W [rows, cols] E4M3, x [cols] bf16.  Bit-identical, row for row, to the
+ * corresponding output of qffn_gemv_dual.  cols % 16 == 0,
+ * 16 <= cols <= 32768, rows >= 1. */
+qffn_status qffn_gemv(uint16_t* out, const uint16_t* x, const uint8_t* w, const float* row_scale,
+                      int64_t rows, int64_t cols, qffn_stream_t stream);
+
+/* ---- Step A7: silu_mul, in place ------------------------------------------
+ * [metrale] silu_mul(gate_out, up_out -> gate_out): g[i] = bf16(silu(g[i]) * u[i]).
+ * n >= 0, n % 8 == 0. */
+qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream_t stream);
+
+/* ---- Whole single-token decode FFN: A6 -> A7 -> A8 ------------------------
+ * [metrale] DenseFfnLayer::forward, FP8 split-SiLU arm.  x [C] bf16 (already
+ * normalised), Wg, Wu [H, C] E4M3 with s_gate, s_up [H]; Wd [C, H] E4M3 with
+ * s_down [C]; out [C] bf16.  workspace >= qffn_decode_workspace_size() bytes
+ * (holds g then u, [H] bf16 each; g holds h after the call).
+ * C % 16 == 0, H % 16 == 0, 16 <= C, H <= 32768. */
+size_t qffn_decode_workspace_size(int64_t C, int64_t H);
+qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
+                                const float* s_gate, const uint8_t* w_up, const float* s_up,
+                                const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
+                                void* workspace, size_t workspace_bytes, qffn_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QFFN_H_ */

@@ -1,0 +1,132 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every
+entry point of include/qffn.h, and the host-side argument checks return the
+documented status codes before anything is enqueued."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qffn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "_qffn_build", os.path.join(ROOT, "transformer_ffn_block_gb300", "_build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    path = b.build()
+    import transformer_ffn_block_gb300 as q
+    assert q.LIB_PATH == path
+    return q
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qffn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ("qffn_rmsnorm_absmax", "qffn_quantize", "qffn_fp8_gemm_scaled", "qffn_swiglu_quant",
+              "qffn_forward", "qffn_decode_forward"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\b(qffn_[a-z0-9_]+)\b", out))
+    missing = [n for n in _declared() if n not in exported]
+    assert not missing, missing
+    for n in _declared():
+        assert hasattr(lib.lib, n)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.qffn_abi_version() == 1
+    for code in range(6):
+        assert lib.qffn_status_string(code)
+    assert lib.qffn_status_string(99) == "unknown status"
+
+
+A = 1 << 20          # a fake, 16-byte-aligned address: checks fail before any use
+MIS = A + 4           # misaligned
+NULL = None
+
+
+def _call(lib, name, *args):
+    return getattr(lib.lib, name)(*args)
+
+
+def test_rmsnorm_argument_checks(lib):
+    f = lambda *a: _call(lib, "qffn_rmsnorm_absmax", *a)
+    ok = (A, A, A, A, A, A, A, 1e-5, 4, 256, None)
+    bad_null = (A, NULL, A, A, A, A, A, 1e-5, 4, 256, None)
+    assert f(*bad_null) == 1
+    assert f(A, A, A, A, A, A, A, -1.0, 4, 256, None) == 1            # eps < 0
+    assert f(A, A, A, A, A, A, A, float("nan"), 4, 256, None) == 1
+    assert f(A, A, A, A, A, A, A, 1e-5, -1, 256, None) == 1
+    assert f(A, A, A, A, A, A, A, 1e-5, 4, 12, None) == 2              # C % 8
+    assert f(A, A, A, A, A, A, A, 1e-5, 4, 16392, None) == 2           # C > 16384
+    assert f(A, MIS, A, A, A, A, A, 1e-5, 4, 256, None) == 3
+    assert f(NULL, A, A, A, A, A, A, 1e-5, 4, 256, None) == 1          # res_in given, res_out NULL
+    del ok
+
+
+def test_gemm_argument_checks(lib):
+    f = lambda *a: _call(lib, "qffn_fp8_gemm_scaled", *a)
+    assert f(A, A, A, A, NULL, 4, 32, 16, None) == 1
+    assert f(A, A, A, A, A, 4, 48, 16, None) == 2     # N % 32
+    assert f(A, A, A, A, A, 4, 32, 24, None) == 2     # K % 16
+    assert f(A, A, A, A, A, 4, 32, 0, None) == 2
+    assert f(A, MIS, A, A, A, 4, 32, 16, None) == 3
+    g = lambda *a: _call(lib, "qffn_gate_up_swiglu", *a)
+    assert g(A, A, A, A, A, A, 4, 256, 200, None) == 2  # H % 128
+    assert g(A, A, A, A, A, A, 4, 20, 256, None) == 2   # C % 16
+
+
+def test_forward_workspace_and_checks(lib):
+    assert lib.qffn_forward_workspace_size(2, 32, 256, 768) > 0
+    assert lib.qffn_forward_workspace_size(2, 32, 200, 768) == 0
+    B, T, C, H = 8, 2048, 4096, 14336
+    off = lib.qffn_forward_workspace_offsets(B, T, C, H)
+    N = B * T
+    assert off[0] == 0 and off[1] >= N * C * 2 and off[2] >= off[1] + N * C
+    assert off[3] >= off[2] + N * H * 2
+    assert lib.qffn_forward_workspace_size(B, T, C, H) >= off[3] + N * H
+    assert all(o % 256 == 0 for o in off)
+    f = lambda *a: _call(lib, "qffn_forward", *a)
+    ws = lib.qffn_forward_workspace_size(2, 32, 256, 768)
+    args = [A, A, A, A, A, A, A, A, 1e-5, A, A, A, A, 2, 32, 256, 768, A, ws, None]
+    bad = list(args); bad[17] = A + 16                         # workspace not 256-aligned
+    assert f(*bad) == 3
+    bad = list(args); bad[18] = ws - 1                         # workspace too small
+    assert f(*bad) == 1
+    bad = list(args); bad[15] = 192                            # C % 128
+    assert f(*bad) == 2
+    bad = list(args); bad[8] = -1.0
+    assert f(*bad) == 1
+
+
+def test_decode_checks(lib):
+    assert lib.qffn_decode_workspace_size(4096, 14336) >= 4 * 14336
+    f = lambda *a: _call(lib, "qffn_decode_forward", *a)
+    ws = lib.qffn_decode_workspace_size(4096, 14336)
+    assert f(A, A, A, A, A, A, A, A, 4096, 14336, A, ws - 2, None) == 1
+    assert f(A, A, A, A, A, A, A, A, 4100, 14336, A, ws, None) == 2
+    assert f(A, MIS, A, A, A, A, A, A, 4096, 14336, A, ws, None) == 3
+    assert _call(lib, "qffn_gemv", A, A, A, A, 10, 24, None) == 2
+    assert _call(lib, "qffn_silu_mul", A, A, 12, None) == 2
+    assert _call(lib, "qffn_quantize_rows", A, A, A, 3, 8, None) == 2
+
+
+def test_python_binding_raises(lib):
+    with pytest.raises(lib.QffnError) as e:
+        lib.qffn_gemv(A, A, A, A, 10, 24, stream=0)
+    assert e.value.status == 2

@@ -1,0 +1,194 @@
+"""Python binding of libqffn (FP8 SwiGLU FFN block for one GB300).
+
+Argument marshalling only: each function here has the name of a C entry
+point of ``include/qffn.h``, turns torch tensors (or raw integer device
+addresses) into pointers, passes the current torch CUDA stream unless one is
+given, and raises ``QffnError`` on a non-zero status.  Every step of the
+block runs in the CUDA kernels of ``libqffn.so``; there is no fallback.  If
+the library is missing the import fails (run ``build()`` first).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as LIB_PATH
+from ._build import build
+
+__all__ = [
+    "QffnError", "lib", "build", "LIB_PATH", "STATUS",
+    "qffn_status_string", "qffn_abi_version", "qffn_check_status",
+    "qffn_rmsnorm_absmax", "qffn_absmax", "qffn_quantize", "qffn_quantize_rows",
+    "qffn_fp8_gemm_scaled", "qffn_gate_up_swiglu", "qffn_swiglu_quant",
+    "qffn_forward_workspace_size", "qffn_forward_workspace_offsets", "qffn_forward",
+    "qffn_gemv_dual", "qffn_gemv", "qffn_silu_mul", "qffn_decode_workspace_size",
+    "qffn_decode_forward",
+]
+
+STATUS = {0: "QFFN_OK", 1: "QFFN_ERR_INVALID_ARG", 2: "QFFN_ERR_UNSUPPORTED_SHAPE",
+          3: "QFFN_ERR_MISALIGNED", 4: "QFFN_ERR_CUDA", 5: "QFFN_ERR_TIMEOUT"}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is not built; run transformer_ffn_block_gb300._build.build() "
+        "(or __graft_entry__.build()) first")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+_S = ctypes.c_int
+
+_SIGS = {
+    "qffn_status_string": ([_S], ctypes.c_char_p),
+    "qffn_abi_version": ([], ctypes.c_int),
+    "qffn_check_status": ([_P], _S),
+    "qffn_rmsnorm_absmax": ([_P, _P, _P, _P, _P, _P, _P, _F, _I64, _I64, _P], _S),
+    "qffn_absmax": ([_P, _P, _I64, _P], _S),
+    "qffn_quantize": ([_P, _P, _P, _I64, _P], _S),
+    "qffn_quantize_rows": ([_P, _P, _P, _I64, _I64, _P], _S),
+    "qffn_fp8_gemm_scaled": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
+    "qffn_gate_up_swiglu": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
+    "qffn_swiglu_quant": ([_P, _P, _P, _P, _I64, _I64, _P], _S),
+    "qffn_forward_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
+    "qffn_forward_workspace_offsets": ([_I64, _I64, _I64, _I64, ctypes.POINTER(_SZ)], _S),
+    "qffn_forward": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P,
+                      _I64, _I64, _I64, _I64, _P, _SZ, _P], _S),
+    "qffn_gemv_dual": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], _S),
+    "qffn_gemv": ([_P, _P, _P, _P, _I64, _I64, _P], _S),
+    "qffn_silu_mul": ([_P, _P, _I64, _P], _S),
+    "qffn_decode_workspace_size": ([_I64, _I64], _SZ),
+    "qffn_decode_forward": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P], _S),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+
+class QffnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({qffn_status_string(status)})")
+
+
+def _ptr(t):
+    """torch tensor -> device address; int -> itself; None -> NULL."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise QffnError(fn, status)
+
+
+def qffn_status_string(status: int) -> str:
+    return lib.qffn_status_string(status).decode()
+
+
+def qffn_abi_version() -> int:
+    return lib.qffn_abi_version()
+
+
+def qffn_check_status(stream=None):
+    _check("qffn_check_status", lib.qffn_check_status(_stream(stream)))
+
+
+def qffn_rmsnorm_absmax(res_out, y, rstd, stats, res_in, x, gain, eps, N, C, stream=None):
+    _check("qffn_rmsnorm_absmax", lib.qffn_rmsnorm_absmax(
+        _ptr(res_out), _ptr(y), _ptr(rstd), _ptr(stats), _ptr(res_in), _ptr(x), _ptr(gain),
+        float(eps), int(N), int(C), _stream(stream)))
+
+
+def qffn_absmax(stats, inp, n, stream=None):
+    _check("qffn_absmax", lib.qffn_absmax(_ptr(stats), _ptr(inp), int(n), _stream(stream)))
+
+
+def qffn_quantize(q, stats, inp, n, stream=None):
+    _check("qffn_quantize", lib.qffn_quantize(_ptr(q), _ptr(stats), _ptr(inp), int(n), _stream(stream)))
+
+
+def qffn_quantize_rows(q, row_scale, w, rows, cols, stream=None):
+    _check("qffn_quantize_rows", lib.qffn_quantize_rows(
+        _ptr(q), _ptr(row_scale), _ptr(w), int(rows), int(cols), _stream(stream)))
+
+
+def qffn_fp8_gemm_scaled(out, a, a_scale, w, w_scale, M, N, K, stream=None):
+    _check("qffn_fp8_gemm_scaled", lib.qffn_fp8_gemm_scaled(
+        _ptr(out), _ptr(a), _ptr(a_scale), _ptr(w), _ptr(w_scale), int(M), int(N), int(K),
+        _stream(stream)))
+
+
+def qffn_gate_up_swiglu(h, stats_h, yq, y_scale, w1, w1_scale, N, C, H, stream=None):
+    _check("qffn_gate_up_swiglu", lib.qffn_gate_up_swiglu(
+        _ptr(h), _ptr(stats_h), _ptr(yq), _ptr(y_scale), _ptr(w1), _ptr(w1_scale),
+        int(N), int(C), int(H), _stream(stream)))
+
+
+def qffn_swiglu_quant(h, hq, stats, gate_up, N, H, stream=None):
+    _check("qffn_swiglu_quant", lib.qffn_swiglu_quant(
+        _ptr(h), _ptr(hq), _ptr(stats), _ptr(gate_up), int(N), int(H), _stream(stream)))
+
+
+def qffn_forward_workspace_size(B, T, C, H) -> int:
+    return int(lib.qffn_forward_workspace_size(int(B), int(T), int(C), int(H)))
+
+
+def qffn_forward_workspace_offsets(B, T, C, H) -> list[int]:
+    off = (_SZ * 4)()
+    _check("qffn_forward_workspace_offsets",
+           lib.qffn_forward_workspace_offsets(int(B), int(T), int(C), int(H), off))
+    return [int(v) for v in off]
+
+
+def qffn_forward(res_out, out, rstd, stats_y, stats_h, res_in, x, gain, eps, w1, w1_scale,
+                 w2, w2_scale, B, T, C, H, workspace, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("qffn_forward", lib.qffn_forward(
+        _ptr(res_out), _ptr(out), _ptr(rstd), _ptr(stats_y), _ptr(stats_h), _ptr(res_in),
+        _ptr(x), _ptr(gain), float(eps), _ptr(w1), _ptr(w1_scale), _ptr(w2), _ptr(w2_scale),
+        int(B), int(T), int(C), int(H), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def qffn_gemv_dual(g, u, x, w_gate, s_gate, w_up, s_up, H, C, stream=None):
+    _check("qffn_gemv_dual", lib.qffn_gemv_dual(
+        _ptr(g), _ptr(u), _ptr(x), _ptr(w_gate), _ptr(s_gate), _ptr(w_up), _ptr(s_up),
+        int(H), int(C), _stream(stream)))
+
+
+def qffn_gemv(out, x, w, row_scale, rows, cols, stream=None):
+    _check("qffn_gemv", lib.qffn_gemv(
+        _ptr(out), _ptr(x), _ptr(w), _ptr(row_scale), int(rows), int(cols), _stream(stream)))
+
+
+def qffn_silu_mul(g, u, n, stream=None):
+    _check("qffn_silu_mul", lib.qffn_silu_mul(_ptr(g), _ptr(u), int(n), _stream(stream)))
+
+
+def qffn_decode_workspace_size(C, H) -> int:
+    return int(lib.qffn_decode_workspace_size(int(C), int(H)))
+
+
+def qffn_decode_forward(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, workspace,
+                        workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("qffn_decode_forward", lib.qffn_decode_forward(
+        _ptr(out), _ptr(x), _ptr(w_gate), _ptr(s_gate), _ptr(w_up), _ptr(s_up), _ptr(w_down),
+        _ptr(s_down), int(C), int(H), _ptr(workspace), int(workspace_bytes), _stream(stream)))

@@ -1,0 +1,268 @@
+// C ABI of libqffn: argument checking and the orchestration of the kernels.
+// The contract of every entry point is stated in include/qffn.h.
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/qffn.h"
+#include "launch.h"
+
+namespace {
+
+using qffn::num_sms;
+
+constexpr int kAbiVersion = 1;
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline qffn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QFFN_OK : QFFN_ERR_CUDA; }
+
+#define QFFN_REQUIRE(cond, err) \
+  do {                          \
+    if (!(cond)) return (err);  \
+  } while (0)
+#define QFFN_PTR(p) QFFN_REQUIRE((p) != nullptr, QFFN_ERR_INVALID_ARG)
+#define QFFN_ALIGNED(p) QFFN_REQUIRE((p) == nullptr || aligned16(p), QFFN_ERR_MISALIGNED)
+#define QFFN_CUDA(expr)                              \
+  do {                                               \
+    cudaError_t e_ = (expr);                         \
+    if (e_ != cudaSuccess) return QFFN_ERR_CUDA;     \
+  } while (0)
+
+constexpr int64_t kMaxDim = int64_t(1) << 20;
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+
+// workspace layout of qffn_forward: y [N,C] bf16 | yq [N,C] e4m3 | h [N,H] bf16 | hq [N,H] e4m3
+void forward_offsets(int64_t N, int64_t C, int64_t H, size_t off[5]) {
+  off[0] = 0;
+  off[1] = round_up(off[0] + size_t(N) * size_t(C) * 2, 256);
+  off[2] = round_up(off[1] + size_t(N) * size_t(C), 256);
+  off[3] = round_up(off[2] + size_t(N) * size_t(H) * 2, 256);
+  off[4] = round_up(off[3] + size_t(N) * size_t(H), 256);
+}
+
+qffn_status check_forward_shape(int64_t B, int64_t T, int64_t C, int64_t H) {
+  QFFN_REQUIRE(B >= 0 && T >= 0 && C >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(B == 0 || T <= kMaxRows / B, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(C % 128 == 0 && C >= 128 && C <= 16384, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(H % 128 == 0 && H >= 128 && H <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  return QFFN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qffn_status_string(qffn_status s) {
+  switch (s) {
+    case QFFN_OK: return "ok";
+    case QFFN_ERR_INVALID_ARG: return "invalid argument";
+    case QFFN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case QFFN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case QFFN_ERR_CUDA: return "CUDA error";
+    case QFFN_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+int qffn_abi_version(void) { return kAbiVersion; }
+
+qffn_status qffn_check_status(qffn_stream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return QFFN_ERR_CUDA;
+  unsigned int st = 0;
+  if (qffn::gemm_take_status(&st) != cudaSuccess) return QFFN_ERR_CUDA;
+  return st != 0 ? QFFN_ERR_TIMEOUT : QFFN_OK;
+}
+
+qffn_status qffn_rmsnorm_absmax(uint16_t* res_out, uint16_t* y, float* rstd, float* stats,
+                                const uint16_t* res_in, const uint16_t* x, const uint16_t* gain,
+                                float eps, int64_t N, int64_t C, qffn_stream_t stream) {
+  QFFN_PTR(y); QFFN_PTR(rstd); QFFN_PTR(x); QFFN_PTR(gain);
+  if (res_in != nullptr) QFFN_PTR(res_out);
+  QFFN_REQUIRE(N >= 0 && C >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(isfinite(eps) && eps >= 0.0f, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(C % 8 == 0 && C >= 8 && C <= 16384, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(y); QFFN_ALIGNED(x); QFFN_ALIGNED(gain); QFFN_ALIGNED(rstd);
+  if (res_in != nullptr) { QFFN_ALIGNED(res_in); QFFN_ALIGNED(res_out); }
+  QFFN_REQUIRE(stats == nullptr || aligned16(stats), QFFN_ERR_MISALIGNED);
+  return from_cuda(qffn::launch_rmsnorm(res_out, y, rstd, stats, res_in, x, gain, eps, N, int(C),
+                                        stream));
+}
+
+qffn_status qffn_absmax(float* stats, const uint16_t* in, int64_t n, qffn_stream_t stream) {
+  QFFN_PTR(stats); QFFN_PTR(in);
+  QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_ALIGNED(stats); QFFN_ALIGNED(in);
+  return from_cuda(qffn::launch_absmax(stats, in, n, stream));
+}
+
+qffn_status qffn_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t n,
+                          qffn_stream_t stream) {
+  QFFN_PTR(q); QFFN_PTR(stats); QFFN_PTR(in);
+  QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_ALIGNED(q); QFFN_ALIGNED(stats); QFFN_ALIGNED(in);
+  return from_cuda(qffn::launch_quantize(q, stats, in, n, stream));
+}
+
+qffn_status qffn_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, int64_t rows,
+                               int64_t cols, qffn_stream_t stream) {
+  QFFN_PTR(q); QFFN_PTR(row_scale); QFFN_PTR(w);
+  QFFN_REQUIRE(rows >= 0 && cols >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(rows <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(cols % 16 == 0 && cols >= 16 && cols <= 65536, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(q); QFFN_ALIGNED(row_scale); QFFN_ALIGNED(w);
+  return from_cuda(qffn::launch_quantize_rows(q, row_scale, w, rows, int(cols), stream));
+}
+
+qffn_status qffn_fp8_gemm_scaled(uint16_t* out, const uint8_t* A, const float* a_scale,
+                                 const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
+                                 int64_t K, qffn_stream_t stream) {
+  QFFN_PTR(out); QFFN_PTR(A); QFFN_PTR(a_scale); QFFN_PTR(W); QFFN_PTR(w_scale);
+  QFFN_REQUIRE(M >= 0 && N >= 0 && K >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(M <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(N % 32 == 0 && N >= 32 && N <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(K % 16 == 0 && K >= 16 && K <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE((M + 127) / 128 * ((N + 255) / 256) < (int64_t(1) << 31), QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(out); QFFN_ALIGNED(A); QFFN_ALIGNED(W);
+  return from_cuda(qffn::launch_gemm_bf16(out, A, a_scale, W, w_scale, M, N, K, stream));
+}
+
+qffn_status qffn_gate_up_swiglu(uint16_t* h, float* stats_h, const uint8_t* yq,
+                                const float* y_scale, const uint8_t* w1, const float* w1_scale,
+                                int64_t N, int64_t C, int64_t H, qffn_stream_t stream) {
+  QFFN_PTR(h); QFFN_PTR(stats_h); QFFN_PTR(yq); QFFN_PTR(y_scale); QFFN_PTR(w1); QFFN_PTR(w1_scale);
+  QFFN_REQUIRE(N >= 0 && C >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(C % 16 == 0 && C >= 16 && C <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(H % 128 == 0 && H >= 128 && H <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE((N + 127) / 128 * (H / 128) < (int64_t(1) << 31), QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(h); QFFN_ALIGNED(stats_h); QFFN_ALIGNED(yq); QFFN_ALIGNED(w1);
+  return from_cuda(qffn::launch_gemm_swiglu(h, stats_h, yq, y_scale, w1, w1_scale, N, H, C, stream));
+}
+
+qffn_status qffn_swiglu_quant(uint16_t* h, uint8_t* hq, float* stats, const uint16_t* gate_up,
+                              int64_t N, int64_t H, qffn_stream_t stream) {
+  QFFN_PTR(hq); QFFN_PTR(stats); QFFN_PTR(gate_up);
+  QFFN_REQUIRE(N >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(H % 8 == 0 && H >= 8 && H <= kMaxDim && N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(h); QFFN_ALIGNED(hq); QFFN_ALIGNED(stats); QFFN_ALIGNED(gate_up);
+  QFFN_CUDA(qffn::launch_swiglu_absmax(h, stats, gate_up, N, H, stream));
+  if (h != nullptr) return from_cuda(qffn::launch_quantize(hq, stats, h, N * H, stream));
+  return from_cuda(qffn::launch_swiglu_requant(hq, stats, gate_up, N, H, stream));
+}
+
+size_t qffn_forward_workspace_size(int64_t B, int64_t T, int64_t C, int64_t H) {
+  if (check_forward_shape(B, T, C, H) != QFFN_OK) return 0;
+  size_t off[5];
+  forward_offsets(B * T, C, H, off);
+  return off[4] > 0 ? off[4] : 256;
+}
+
+qffn_status qffn_forward_workspace_offsets(int64_t B, int64_t T, int64_t C, int64_t H,
+                                           size_t offsets[4]) {
+  QFFN_PTR(offsets);
+  const qffn_status st = check_forward_shape(B, T, C, H);
+  if (st != QFFN_OK) return st;
+  size_t off[5];
+  forward_offsets(B * T, C, H, off);
+  for (int i = 0; i < 4; ++i) offsets[i] = off[i];
+  return QFFN_OK;
+}
+
+qffn_status qffn_forward(uint16_t* res_out, uint16_t* out, float* rstd, float* stats_y,
+                         float* stats_h, const uint16_t* res_in, const uint16_t* x,
+                         const uint16_t* gain, float eps, const uint8_t* w1,
+                         const float* w1_scale, const uint8_t* w2, const float* w2_scale,
+                         int64_t B, int64_t T, int64_t C, int64_t H, void* workspace,
+                         size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_PTR(out); QFFN_PTR(rstd); QFFN_PTR(stats_y); QFFN_PTR(stats_h); QFFN_PTR(x);
+  QFFN_PTR(gain); QFFN_PTR(w1); QFFN_PTR(w1_scale); QFFN_PTR(w2); QFFN_PTR(w2_scale);
+  QFFN_PTR(workspace);
+  if (res_in != nullptr) QFFN_PTR(res_out);
+  QFFN_REQUIRE(isfinite(eps) && eps >= 0.0f, QFFN_ERR_INVALID_ARG);
+  const qffn_status st = check_forward_shape(B, T, C, H);
+  if (st != QFFN_OK) return st;
+  const int64_t N = B * T;
+  size_t off[5];
+  forward_offsets(N, C, H, off);
+  QFFN_REQUIRE(workspace_bytes >= off[4], QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(aligned256(workspace), QFFN_ERR_MISALIGNED);
+  QFFN_ALIGNED(out); QFFN_ALIGNED(rstd); QFFN_ALIGNED(stats_y); QFFN_ALIGNED(stats_h);
+  QFFN_ALIGNED(x); QFFN_ALIGNED(gain); QFFN_ALIGNED(w1); QFFN_ALIGNED(w2);
+  if (res_in != nullptr) { QFFN_ALIGNED(res_in); QFFN_ALIGNED(res_out); }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* y = reinterpret_cast<uint16_t*>(ws + off[0]);
+  uint8_t* yq = ws + off[1];
+  uint16_t* h = reinterpret_cast<uint16_t*>(ws + off[2]);
+  uint8_t* hq = ws + off[3];
+
+  // A1: r, y, rstd, stats_y[0]
+  QFFN_CUDA(qffn::launch_rmsnorm(res_out, y, rstd, stats_y, res_in, x, gain, eps, N, int(C), stream));
+  // A2: yq, stats_y[1]
+  QFFN_CUDA(qffn::launch_quantize(yq, stats_y, y, N * C, stream));
+  // A3 + A4: h, stats_h[0]
+  QFFN_CUDA(qffn::launch_gemm_swiglu(h, stats_h, yq, stats_y + 1, w1, w1_scale, N, H, C, stream));
+  // A4 requantisation: hq, stats_h[1]
+  QFFN_CUDA(qffn::launch_quantize(hq, stats_h, h, N * H, stream));
+  // A5: out
+  return from_cuda(qffn::launch_gemm_bf16(out, hq, stats_h + 1, w2, w2_scale, N, C, H, stream));
+}
+
+qffn_status qffn_gemv_dual(uint16_t* g, uint16_t* u, const uint16_t* x, const uint8_t* w_gate,
+                           const float* s_gate, const uint8_t* w_up, const float* s_up,
+                           int64_t H, int64_t C, qffn_stream_t stream) {
+  QFFN_PTR(g); QFFN_PTR(u); QFFN_PTR(x); QFFN_PTR(w_gate); QFFN_PTR(s_gate); QFFN_PTR(w_up); QFFN_PTR(s_up);
+  QFFN_REQUIRE(H >= 1 && C >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(C % 16 == 0 && C >= 16 && C <= 32768 && H <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(x); QFFN_ALIGNED(w_gate); QFFN_ALIGNED(w_up);
+  return from_cuda(qffn::launch_gemv(g, u, x, w_gate, s_gate, w_up, s_up, H, C, false, stream));
+}
+
+qffn_status qffn_gemv(uint16_t* out, const uint16_t* x, const uint8_t* w, const float* row_scale,
+                      int64_t rows, int64_t cols, qffn_stream_t stream) {
+  QFFN_PTR(out); QFFN_PTR(x); QFFN_PTR(w); QFFN_PTR(row_scale);
+  QFFN_REQUIRE(rows >= 1 && cols >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(cols % 16 == 0 && cols >= 16 && cols <= 32768 && rows <= kMaxRows,
+               QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(x); QFFN_ALIGNED(w);
+  return from_cuda(qffn::launch_gemv(out, nullptr, x, w, row_scale, nullptr, nullptr, rows, cols,
+                                     false, stream));
+}
+
+qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream_t stream) {
+  QFFN_PTR(g); QFFN_PTR(u);
+  QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(n % 8 == 0, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(g); QFFN_ALIGNED(u);
+  return from_cuda(qffn::launch_silu_mul(g, u, n, false, stream));
+}
+
+size_t qffn_decode_workspace_size(int64_t C, int64_t H) {
+  if (C < 16 || H < 16 || C > 32768 || H > 32768) return 0;
+  return round_up(size_t(H) * 2, 256) + size_t(H) * 2;
+}
+
+qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
+                                const float* s_gate, const uint8_t* w_up, const float* s_up,
+                                const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
+                                void* workspace, size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_PTR(out); QFFN_PTR(x); QFFN_PTR(w_gate); QFFN_PTR(s_gate); QFFN_PTR(w_up); QFFN_PTR(s_up);
+  QFFN_PTR(w_down); QFFN_PTR(s_down); QFFN_PTR(workspace);
+  QFFN_REQUIRE(C % 16 == 0 && H % 16 == 0 && C >= 16 && H >= 16 && C <= 32768 && H <= 32768,
+               QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(workspace_bytes >= qffn_decode_workspace_size(C, H), QFFN_ERR_INVALID_ARG);
+  QFFN_ALIGNED(out); QFFN_ALIGNED(x); QFFN_ALIGNED(w_gate); QFFN_ALIGNED(w_up); QFFN_ALIGNED(w_down);
+  QFFN_ALIGNED(workspace);
+  uint16_t* g = static_cast<uint16_t*>(workspace);
+  uint16_t* u = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + round_up(size_t(H) * 2, 256));
+  // A6 (stream-ordered after the caller's producer of x), then A7 and A8 as
+  // programmatic dependent launches so each launch overlaps its predecessor's tail.
+  QFFN_CUDA(qffn::launch_gemv(g, u, x, w_gate, s_gate, w_up, s_up, H, C, false, stream));
+  QFFN_CUDA(qffn::launch_silu_mul(g, u, H, true, stream));
+  return from_cuda(qffn::launch_gemv(out, nullptr, g, w_down, s_down, nullptr, nullptr, C, H, true, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,101 @@
+// Shared device helpers for the qffn kernels (sm_103a).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define QFFN_DEVI __device__ __forceinline__
+
+namespace qffn {
+
+constexpr int kNumSMsHint = 152;
+
+// ----------------------------------------------------------------- bf16 bits
+QFFN_DEVI float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+QFFN_DEVI float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+QFFN_DEVI float bf16_to_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+// fp32 -> bf16, round to nearest even (the cvt instruction; finite inputs).
+QFFN_DEVI uint16_t f32_to_bf16(float f) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
+}
+// Two fp32 -> packed bf16x2 (lo in the low half).
+QFFN_DEVI uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Round through bf16 and back.
+QFFN_DEVI float round_bf16(float f) { return bf16_to_f32(f32_to_bf16(f)); }
+
+// ----------------------------------------------------------------- e4m3
+// Two fp32 -> packed E4M3x2 (lo in the low byte), nearest even, saturating.
+QFFN_DEVI uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// 4 packed E4M3 codes -> 4 floats (exact), via the e4m3x2 -> f16x2 cvt.
+QFFN_DEVI void e4m3x4_to_f32(uint32_t w, float& f0, float& f1, float& f2, float& f3) {
+  uint32_t h01, h23;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(uint16_t(w & 0xFFFF)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(uint16_t(w >> 16)));
+  __half2 a = *reinterpret_cast<__half2*>(&h01);
+  __half2 b = *reinterpret_cast<__half2*>(&h23);
+  float2 fa = __half22float2(a), fb = __half22float2(b);
+  f0 = fa.x; f1 = fa.y; f2 = fb.x; f3 = fb.y;
+}
+
+// ----------------------------------------------------------------- SwiGLU
+// silu(g) * u in fp32.  silu(g) = g * sigmoid(g); the sigmoid is formed from
+// e = exp(-|g|) in (0, 1] so neither branch overflows:
+//   g >= 0: 1 / (1 + e);   g < 0: e / (1 + e).
+QFFN_DEVI float silu_mul_f32(float g, float u) {
+  float e = __expf(-fabsf(g));
+  float r = __fdividef(1.0f, 1.0f + e);
+  float sig = g >= 0.0f ? r : e * r;
+  return (g * sig) * u;
+}
+
+// ----------------------------------------------------------------- abs-max
+// Non-negative floats order like their bit patterns as unsigned integers, so
+// a tensor abs-max is an atomicMax on the bits.
+QFFN_DEVI void atomic_max_nonneg(float* addr, float v) {
+  atomicMax(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
+}
+
+QFFN_DEVI float warp_max(float v) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
+}
+
+QFFN_DEVI float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// 16-byte global loads / stores.
+// ld16_ro: data that no thread writes during the kernel (weights, gain).
+// ld16_once: plain coherent load (activations that a call may overwrite in
+// place afterwards; a plain load keeps the compiler's aliasing order).
+QFFN_DEVI uint4 ld16_ro(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
+QFFN_DEVI uint4 ld16_ro_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+QFFN_DEVI uint4 ld16_once(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+QFFN_DEVI void stg16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
+
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// let the next kernel start launching.  Both are no-ops without the launch
+// attribute.
+QFFN_DEVI void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+QFFN_DEVI void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+}  // namespace qffn

@@ -1,0 +1,381 @@
+// HBM-bound kernels of the FFN block: fused residual + RMSNorm + abs-max,
+// tensor abs-max, per-tensor and per-row E4M3 quantisation, SwiGLU with
+// abs-max, SwiGLU requantisation and the decode silu_mul.
+//
+// All of them move 16-byte vectors per thread, reduce in registers, then by
+// warp shuffles and one shared-memory step per block, and record a tensor
+// abs-max with one atomicMax per block on the bits of a non-negative float.
+#include "common.cuh"
+#include "launch.h"
+
+namespace qffn {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+int g_sm_count[64] = {0};
+
+__device__ __forceinline__ float block_reduce_max(float v, float* red) {
+  v = warp_max(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = 0.0f;
+  if (warp == 0) {
+    r = lane < (int)(blockDim.x >> 5) ? red[lane] : 0.0f;
+    r = warp_max(r);
+  }
+  return r;  // valid in warp 0
+}
+
+// ------------------------------------------------------------------ A1
+// One block of 128 threads per row; thread t owns the 16-byte chunks
+// t, t+128, ... of the row and keeps its residual sums in registers between
+// the sum-of-squares pass and the normalisation pass.
+template <int V>
+__global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_t* y, float* rstd,
+                                                      float* stats, const uint16_t* res_in,
+                                                      const uint16_t* x, const uint16_t* gain,
+                                                      float eps, int C) {
+  __shared__ float red[4];
+  const int64_t row = blockIdx.x;
+  const int nchunk = C >> 3;
+  const int tid = threadIdx.x;
+  const size_t base = size_t(row) * size_t(C);
+  uint4 rv[V];
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int c = tid + i * 128;
+    if (c < nchunk) {
+      uint4 xv = ld16_once(x + base + size_t(c) * 8);
+      uint4 r = xv;
+      if (res_in != nullptr) {
+        uint4 a = ld16_once(res_in + base + size_t(c) * 8);
+        // bf16 + bf16 in fp32, one rounding to bf16 (equals rounding the exact sum)
+        r.x = pack_bf16x2(bf16_lo(a.x) + bf16_lo(xv.x), bf16_hi(a.x) + bf16_hi(xv.x));
+        r.y = pack_bf16x2(bf16_lo(a.y) + bf16_lo(xv.y), bf16_hi(a.y) + bf16_hi(xv.y));
+        r.z = pack_bf16x2(bf16_lo(a.z) + bf16_lo(xv.z), bf16_hi(a.z) + bf16_hi(xv.z));
+        r.w = pack_bf16x2(bf16_lo(a.w) + bf16_lo(xv.w), bf16_hi(a.w) + bf16_hi(xv.w));
+        stg16(res_out + base + size_t(c) * 8, r);
+      }
+      rv[i] = r;
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
+        ss = fmaf(lo, lo, ss);
+        ss = fmaf(hi, hi, ss);
+      }
+    }
+  }
+  // block sum of squares
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  const float total = (red[0] + red[1]) + (red[2] + red[3]);
+  const float rs = 1.0f / sqrtf(total / float(C) + eps);
+  if (tid == 0) rstd[row] = rs;
+
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int c = tid + i * 128;
+    if (c < nchunk) {
+      const uint4 g = ld16_ro(gain + size_t(c) * 8);
+      const uint32_t rw[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float lo = (bf16_lo(rw[j]) * rs) * bf16_lo(gw[j]);
+        const float hi = (bf16_hi(rw[j]) * rs) * bf16_hi(gw[j]);
+        o[j] = pack_bf16x2(lo, hi);
+        amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(o[j])), fabsf(bf16_hi(o[j]))));
+      }
+      stg16(y + base + size_t(c) * 8, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+  }
+  if (stats != nullptr) {
+    __syncthreads();  // red[] reuse
+    const float m = block_reduce_max(amax, red);
+    if (tid == 0) atomic_max_nonneg(stats, m);
+  }
+}
+
+// ------------------------------------------------------------------ abs-max
+__global__ void __launch_bounds__(kThreads) absmax_kernel(float* stats, const uint16_t* in,
+                                                          int64_t n) {
+  __shared__ float red[kThreads / 32];
+  float m = 0.0f;
+  const int64_t nchunk = n >> 3;
+  for (int64_t c = int64_t(blockIdx.x) * kThreads + threadIdx.x; c < nchunk;
+       c += int64_t(gridDim.x) * kThreads) {
+    const uint4 v = ld16_ro_stream(in + c * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+  if (blockIdx.x == 0) {
+    for (int64_t i = nchunk * 8 + threadIdx.x; i < n; i += kThreads) m = fmaxf(m, fabsf(bf16_to_f32(in[i])));
+  }
+  m = block_reduce_max(m, red);
+  if (threadIdx.x == 0) atomic_max_nonneg(stats, m);
+}
+
+// ------------------------------------------------------------------ A2
+// 16 elements per thread per step: two 16-byte loads, one 16-byte store.
+__global__ void __launch_bounds__(kThreads) quantize_kernel(uint8_t* q, float* stats,
+                                                            const uint16_t* in, int64_t n) {
+  const float amax = stats[0];
+  const bool zero = !(amax > 0.0f);
+  const float inv = zero ? 0.0f : 448.0f / amax;
+  if (blockIdx.x == 0 && threadIdx.x == 0) stats[1] = zero ? 1.0f : amax / 448.0f;
+  const int64_t nchunk = n >> 4;
+  for (int64_t c = int64_t(blockIdx.x) * kThreads + threadIdx.x; c < nchunk;
+       c += int64_t(gridDim.x) * kThreads) {
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (!zero) {
+      const uint4 a = ld16_once(in + c * 16);
+      const uint4 b = ld16_once(in + c * 16 + 8);
+      const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint16_t lo = f32x2_to_e4m3x2(bf16_lo(w[2 * j]) * inv, bf16_hi(w[2 * j]) * inv);
+        const uint16_t hi = f32x2_to_e4m3x2(bf16_lo(w[2 * j + 1]) * inv, bf16_hi(w[2 * j + 1]) * inv);
+        p[j] = uint32_t(lo) | (uint32_t(hi) << 16);
+      }
+      o = make_uint4(p[0], p[1], p[2], p[3]);
+    }
+    stg16(q + c * 16, o);
+  }
+  if (blockIdx.x == 0) {
+    for (int64_t i = nchunk * 16 + threadIdx.x; i < n; i += kThreads) {
+      const uint16_t v = zero ? 0 : f32x2_to_e4m3x2(bf16_to_f32(in[i]) * inv, 0.0f);
+      q[i] = uint8_t(v & 0xFF);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ per-row records
+// One block per row: the row abs-max, then the row quantised with it.
+__global__ void __launch_bounds__(kThreads) quantize_rows_kernel(uint8_t* q, float* row_scale,
+                                                                 const uint16_t* w, int cols) {
+  __shared__ float red[kThreads / 32];
+  __shared__ float s_amax;
+  const int64_t row = blockIdx.x;
+  const uint16_t* src = w + size_t(row) * cols;
+  uint8_t* dst = q + size_t(row) * cols;
+  const int nchunk = cols >> 4;
+  float m = 0.0f;
+  for (int c = threadIdx.x; c < nchunk; c += kThreads) {
+    const uint4 a = ld16_ro(src + c * 16), b = ld16_ro(src + c * 16 + 8);
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(v[j])), fabsf(bf16_hi(v[j]))));
+  }
+  m = block_reduce_max(m, red);
+  if (threadIdx.x == 0) s_amax = m;
+  __syncthreads();
+  const float amax = s_amax;
+  const bool zero = !(amax > 0.0f);
+  const float inv = zero ? 0.0f : 448.0f / amax;
+  if (threadIdx.x == 0) row_scale[row] = zero ? 1.0f : amax / 448.0f;
+  for (int c = threadIdx.x; c < nchunk; c += kThreads) {
+    uint4 o = make_uint4(0, 0, 0, 0);
+    if (!zero) {
+      const uint4 a = ld16_ro(src + c * 16), b = ld16_ro(src + c * 16 + 8);
+      const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t p[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint16_t lo = f32x2_to_e4m3x2(bf16_lo(v[2 * j]) * inv, bf16_hi(v[2 * j]) * inv);
+        const uint16_t hi = f32x2_to_e4m3x2(bf16_lo(v[2 * j + 1]) * inv, bf16_hi(v[2 * j + 1]) * inv);
+        p[j] = uint32_t(lo) | (uint32_t(hi) << 16);
+      }
+      o = make_uint4(p[0], p[1], p[2], p[3]);
+    }
+    stg16(dst + c * 16, o);
+  }
+}
+
+// ------------------------------------------------------------------ A4 (standalone)
+// 8 outputs per thread per step: 16 bytes of gate, 16 bytes of up.
+__device__ __forceinline__ uint4 swiglu8(uint4 g, uint4 u) {
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    o[j] = pack_bf16x2(silu_mul_f32(bf16_lo(gw[j]), bf16_lo(uw[j])),
+                       silu_mul_f32(bf16_hi(gw[j]), bf16_hi(uw[j])));
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float absmax8(uint4 v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float m = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  return m;
+}
+
+__global__ void __launch_bounds__(kThreads) swiglu_absmax_kernel(uint16_t* h, float* stats,
+                                                                 const uint16_t* gu, int64_t N,
+                                                                 int64_t H) {
+  __shared__ float red[kThreads / 32];
+  const int64_t per_row = H >> 3;
+  const int64_t total = N * per_row;
+  float m = 0.0f;
+  for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * kThreads) {
+    const int64_t row = i / per_row, c = i - row * per_row;
+    const uint16_t* src = gu + row * 2 * H + c * 8;
+    const uint4 hv = swiglu8(ld16_ro_stream(src), ld16_ro_stream(src + H));
+    m = fmaxf(m, absmax8(hv));
+    if (h != nullptr) stg16(h + row * H + c * 8, hv);
+  }
+  m = block_reduce_max(m, red);
+  if (threadIdx.x == 0) atomic_max_nonneg(stats, m);
+}
+
+__global__ void __launch_bounds__(kThreads) swiglu_requant_kernel(uint8_t* hq, float* stats,
+                                                                  const uint16_t* gu, int64_t N,
+                                                                  int64_t H) {
+  const float amax = stats[0];
+  const bool zero = !(amax > 0.0f);
+  const float inv = zero ? 0.0f : 448.0f / amax;
+  if (blockIdx.x == 0 && threadIdx.x == 0) stats[1] = zero ? 1.0f : amax / 448.0f;
+  const int64_t per_row = H >> 3;
+  const int64_t total = N * per_row;
+  for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * kThreads) {
+    const int64_t row = i / per_row, c = i - row * per_row;
+    const uint16_t* src = gu + row * 2 * H + c * 8;
+    uint2 o = make_uint2(0, 0);
+    if (!zero) {
+      const uint4 hv = swiglu8(ld16_ro_stream(src), ld16_ro_stream(src + H));
+      const uint32_t w[4] = {hv.x, hv.y, hv.z, hv.w};
+      uint32_t p[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint16_t lo = f32x2_to_e4m3x2(bf16_lo(w[2 * j]) * inv, bf16_hi(w[2 * j]) * inv);
+        const uint16_t hi = f32x2_to_e4m3x2(bf16_lo(w[2 * j + 1]) * inv, bf16_hi(w[2 * j + 1]) * inv);
+        p[j] = uint32_t(lo) | (uint32_t(hi) << 16);
+      }
+      o = make_uint2(p[0], p[1]);
+    }
+    *reinterpret_cast<uint2*>(hq + row * H + c * 8) = o;
+  }
+}
+
+// ------------------------------------------------------------------ A7
+__global__ void __launch_bounds__(kThreads) silu_mul_kernel(uint16_t* g, const uint16_t* u,
+                                                            int64_t n) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t nchunk = n >> 3;
+  for (int64_t c = int64_t(blockIdx.x) * kThreads + threadIdx.x; c < nchunk;
+       c += int64_t(gridDim.x) * kThreads) {
+    const uint4 hv = swiglu8(ld16_once(g + c * 8), ld16_once(u + c * 8));
+    stg16(g + c * 8, hv);
+  }
+}
+
+int grid_for(int64_t work_items, int blocks_per_sm) {
+  const int64_t cap = int64_t(num_sms()) * blocks_per_sm;
+  int64_t need = (work_items + kThreads - 1) / kThreads;
+  if (need < 1) need = 1;
+  return int(need < cap ? need : cap);
+}
+
+}  // namespace
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kNumSMsHint;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = kNumSMsHint;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+cudaError_t launch_rmsnorm(uint16_t* res_out, uint16_t* y, float* rstd, float* stats,
+                           const uint16_t* res_in, const uint16_t* x, const uint16_t* gain,
+                           float eps, int64_t N, int C, cudaStream_t s) {
+  if (stats != nullptr) {
+    cudaError_t e = cudaMemsetAsync(stats, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+  }
+  if (N == 0) return cudaSuccess;
+  const int per_thread = (C / 8 + 127) / 128;
+  const dim3 grid(static_cast<unsigned>(N));
+  if (per_thread <= 1)
+    rmsnorm_kernel<1><<<grid, 128, 0, s>>>(res_out, y, rstd, stats, res_in, x, gain, eps, C);
+  else if (per_thread <= 2)
+    rmsnorm_kernel<2><<<grid, 128, 0, s>>>(res_out, y, rstd, stats, res_in, x, gain, eps, C);
+  else if (per_thread <= 4)
+    rmsnorm_kernel<4><<<grid, 128, 0, s>>>(res_out, y, rstd, stats, res_in, x, gain, eps, C);
+  else if (per_thread <= 8)
+    rmsnorm_kernel<8><<<grid, 128, 0, s>>>(res_out, y, rstd, stats, res_in, x, gain, eps, C);
+  else
+    rmsnorm_kernel<16><<<grid, 128, 0, s>>>(res_out, y, rstd, stats, res_in, x, gain, eps, C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_absmax(float* stats, const uint16_t* in, int64_t n, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(stats, 0, sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  if (n == 0) return cudaSuccess;
+  absmax_kernel<<<grid_for(n / 8 + 1, 8), kThreads, 0, s>>>(stats, in, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t n,
+                            cudaStream_t s) {
+  quantize_kernel<<<grid_for(n / 16 + 1, 8), kThreads, 0, s>>>(q, stats, in, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, int64_t rows,
+                                 int cols, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  quantize_rows_kernel<<<unsigned(rows), kThreads, 0, s>>>(q, row_scale, w, cols);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_absmax(uint16_t* h, float* stats, const uint16_t* gate_up, int64_t N,
+                                 int64_t H, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(stats, 0, sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  if (N == 0) return cudaSuccess;
+  swiglu_absmax_kernel<<<grid_for(N * (H / 8), 8), kThreads, 0, s>>>(h, stats, gate_up, N, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_requant(uint8_t* hq, float* stats, const uint16_t* gate_up, int64_t N,
+                                  int64_t H, cudaStream_t s) {
+  swiglu_requant_kernel<<<grid_for(N * (H / 8) + 1, 8), kThreads, 0, s>>>(hq, stats, gate_up, N, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, bool pdl, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_for(n / 8, 4));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, silu_mul_kernel, g, u, n);
+}
+
+}  // namespace qffn

@@ -1,0 +1,482 @@
+// Scaled FP8 (E4M3) GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+//   gemm_bf16   : out[M,N]  = bf16(sA*sW * A[M,K] . W[N,K]^T)
+//   gemm_swiglu : h[M,H]    = bf16(silu(g)*u), g / u the bf16-rounded gate and
+//                 up products of W1 = [2H, K] (gate rows [0,H), up rows
+//                 [H,2H)); the tensor abs-max of h is recorded on the way.
+//
+// These are the two matmuls of the FFN half of llmq "llama_model.cpp",
+// LLamaModel::_forward_block (forward_qmm -> matmul with weight and
+// activation scales; the up projection followed by swiglu_forward).
+//
+// Design (one persistent CTA per SM, 192 threads, warp-specialised):
+//   warp 0      TMA producer: 128x128-byte A tiles and two 128x128-byte B
+//               tiles per stage, 128-byte swizzle, into a 4-stage ring.
+//   warp 1      allocates 512 TMEM columns; one thread issues
+//               tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32) and commits
+//               stage / accumulator barriers.
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
+//               quarter per warp, one output row per thread), scaling,
+//               bf16 rounding, SwiGLU, abs-max, 16-byte stores.
+// Two 256-column accumulators in TMEM let the epilogue of tile i overlap the
+// MMAs of tile i+1.  For the SwiGLU form the 256 B rows of a stage are the
+// 128 gate rows followed by the 128 matching up rows, so one N=256 MMA yields
+// gate in accumulator columns [0,128) and up in [128,256).
+//
+// Every mbarrier wait is bounded (about 2 s on %globaltimer); a wait that
+// runs out raises a CTA abort flag and the device status word, all roles
+// leave their loops, in-flight TMA loads and MMAs are drained (again
+// bounded), TMEM is freed and the kernel returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace qffn {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;        // bytes (= E4M3 elements) of K per stage: one swizzle atom row
+constexpr int UMMA_K = 32;     // K of one kind::f8f6f4 MMA
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;
+constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + NUM_BARS * 8 + 16;
+constexpr int GROUP_M = 16;    // tile raster: 16 M-blocks sweep the N-blocks together
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr unsigned long long kDrainLimitNs = 200000000ull;
+
+// Instruction descriptor of tcgen05.mma.kind::f8f6f4: D f32 (bits 4-5 = 1),
+// A and B E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+__device__ unsigned int g_status;
+
+struct GemmArgs {
+  uint16_t* out;
+  const float* a_scale;
+  const float* w_scale;
+  float* amax;
+  int M, N, K;   // N: output columns (SwiGLU: H)
+  int H;         // SwiGLU: first up row of W1
+  int tiles_m, tiles_n, num_tiles, num_kb;
+};
+
+QFFN_DEVI uint32_t smem_u32(const void* p) { return uint32_t(__cvta_generic_to_shared(p)); }
+
+QFFN_DEVI void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+QFFN_DEVI void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+QFFN_DEVI void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+QFFN_DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+QFFN_DEVI unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase of `bar` with the given parity to complete.  Returns
+// false if the CTA abort flag is up (when honoured) or the time limit runs
+// out; running out raises the abort flag and the device status word.
+QFFN_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                         bool honour_abort = true, unsigned long long limit = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (honour_abort && *abort_flag) return false;
+      if (globaltimer() - t0 > limit) {
+        *abort_flag = 1;
+        atomicOr(&g_status, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+QFFN_DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+QFFN_DEVI void tma_prefetch_desc(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+QFFN_DEVI void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+QFFN_DEVI void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte
+// swizzle layout written by TMA: rows of 128 B, 8-row groups 1024 B apart
+// (stride byte offset), leading byte offset unused for this layout (16 B),
+// descriptor version 1 (bit 46), swizzle mode 2 = 128 B (bits 61-63).
+QFFN_DEVI uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t(16 >> 4) << 16;
+  d |= uint64_t(1024 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+QFFN_DEVI void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+QFFN_DEVI void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+QFFN_DEVI void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+QFFN_DEVI void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
+  const int per_group = GROUP_M * a.tiles_n;
+  const int group = tile / per_group;
+  const int first_m = group * GROUP_M;
+  const int gsize = min(a.tiles_m - first_m, GROUP_M);
+  const int r = tile - group * per_group;
+  mb = first_m + r % gsize;
+  nb = r / gsize;
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * uint32_t(s); };
+  auto empty_bar = [&](int s) { return bar0 + 8u * uint32_t(STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t issued = 0, issued_parity = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, args, mb, nb);
+        const int rowA = mb * BM;
+        const int rowB0 = SWIGLU ? nb * 128 : nb * BN;
+        const int rowB1 = SWIGLU ? args.H + nb * 128 : nb * BN + 128;
+        for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = uint32_t(it / STAGES) & 1u;
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_expect_tx(full_bar(s), STAGE_BYTES);
+          const uint32_t a_dst = smem_u32(sA + s * A_BYTES);
+          const uint32_t b_dst = smem_u32(sB + s * B_BYTES);
+          tma_load_2d(a_dst, &tmA, full_bar(s), kb * BK, rowA);
+          tma_load_2d(b_dst, &tmB, full_bar(s), kb * BK, rowB0);
+          tma_load_2d(b_dst + 128 * BK, &tmB, full_bar(s), kb * BK, rowB1);
+          issued |= 1u << s;
+          issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+        }
+      }
+      // drain: every load this thread issued has landed before smem is released
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s))
+          mbar_wait(full_bar(s), (issued_parity >> s) & 1u, abort_flag, false, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t aph = uint32_t(local >> 1) & 1u;
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = uint32_t(it / STAGES) & 1u;
+          if (!mbar_wait(full_bar(s), ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + s * A_BYTES);
+          const uint32_t b0 = smem_u32(sB + s * B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk)
+            mma_f8(d_tmem, sdesc_sw128(a0 + kk * UMMA_K), sdesc_sw128(b0 + kk * UMMA_K),
+                   uint32_t(kb | kk));
+          mma_commit(empty_bar(s));
+        }
+        if (!ok) break;
+        mma_commit(tfull_bar(acc));
+      }
+      // drain: all MMAs issued by this thread have completed
+      mma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, abort_flag, false, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;                  // TMEM lane quarter of this warp
+    const int row_in_tile = q * 32 + lane;
+    const float scale = args.a_scale[0] * args.w_scale[0];
+    float amax = 0.0f;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t aph = uint32_t(local >> 1) & 1u;
+      if (!mbar_wait(tfull_bar(acc), aph, abort_flag)) break;
+      tc_fence_after();
+      int mb, nb;
+      tile_coords(tile, args, mb, nb);
+      const int row = mb * BM + row_in_tile;
+      const bool row_ok = row < args.M;
+      const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
+      if (!SWIGLU) {
+        uint16_t* orow = args.out + size_t(row) * size_t(args.N);
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tbase + uint32_t(c0), v);
+          const int col = nb * BN + c0;
+          if (row_ok && col < args.N) {
+            uint32_t p[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              p[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * scale,
+                                 __uint_as_float(v[2 * j + 1]) * scale);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              stg16(orow + col + 8 * j, make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+          }
+        }
+      } else {
+        uint16_t* hrow = args.out + size_t(row) * size_t(args.N) + size_t(nb) * 128;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld32x2(tbase + uint32_t(c0), tbase + uint32_t(128 + c0), g, u);
+          uint32_t p[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g0 = round_bf16(__uint_as_float(g[2 * j]) * scale);
+            const float g1 = round_bf16(__uint_as_float(g[2 * j + 1]) * scale);
+            const float u0 = round_bf16(__uint_as_float(u[2 * j]) * scale);
+            const float u1 = round_bf16(__uint_as_float(u[2 * j + 1]) * scale);
+            p[j] = pack_bf16x2(silu_mul_f32(g0, u0), silu_mul_f32(g1, u1));
+            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              stg16(hrow + c0 + 8 * j, make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+    }
+    if (SWIGLU) {
+      amax = warp_max(amax);
+      if (lane == 0) atomic_max_nonneg(args.amax, amax);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D E4M3 tensor [rows, k] (k contiguous), boxes of 128 rows x 128 bytes.
+bool make_map(CUtensorMap* map, const uint8_t* ptr, int64_t rows, int64_t k) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(k), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(k)};
+  cuuint32_t box[2] = {cuuint32_t(BK), 128u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SWIGLU>
+cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s) {
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+    e = cudaFuncSetAttribute(gemm_fp8_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done[dev] = 1;
+  }
+  const int grid = a.num_tiles < num_sms() ? a.num_tiles : num_sms();
+  gemm_fp8_kernel<SWIGLU><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ma, mb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
+                             const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
+                             int64_t K, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M, K) || !make_map(&mb, W, N, K)) return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.out = out;
+  a.a_scale = a_scale;
+  a.w_scale = w_scale;
+  a.amax = nullptr;
+  a.M = int(M);
+  a.N = int(N);
+  a.K = int(K);
+  a.H = 0;
+  a.tiles_m = int((M + BM - 1) / BM);
+  a.tiles_n = int((N + BN - 1) / BN);
+  a.num_tiles = a.tiles_m * a.tiles_n;
+  a.num_kb = int((K + BK - 1) / BK);
+  return launch<false>(ma, mb, a, s);
+}
+
+cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, const float* a_scale,
+                               const uint8_t* W1, const float* w_scale, int64_t M, int64_t H,
+                               int64_t K, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(stats_h, 0, sizeof(float), s);
+  if (e != cudaSuccess || M == 0) return e;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, A, M, K) || !make_map(&mb, W1, 2 * H, K)) return cudaErrorInvalidValue;
+  GemmArgs a{};
+  a.out = h;
+  a.a_scale = a_scale;
+  a.w_scale = w_scale;
+  a.amax = stats_h;
+  a.M = int(M);
+  a.N = int(H);
+  a.K = int(K);
+  a.H = int(H);
+  a.tiles_m = int((M + BM - 1) / BM);
+  a.tiles_n = int(H / 128);
+  a.num_tiles = a.tiles_m * a.tiles_n;
+  a.num_kb = int((K + BK - 1) / BK);
+  return launch<true>(ma, mb, a, s);
+}
+
+cudaError_t gemm_take_status(unsigned int* status) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_status, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (v != 0) e = cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+  *status = v;
+  return e;
+}
+
+}  // namespace qffn

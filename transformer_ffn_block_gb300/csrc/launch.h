@@ -1,0 +1,51 @@
+// Internal launchers of the qffn kernels.  Each enqueues work on `s` and
+// returns the CUDA error of the launch; argument checking is done by the
+// C-ABI layer (api.cu) before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qffn {
+
+// Number of SMs of the current device (cached per device).
+int num_sms();
+
+// ---- elementwise / reduction kernels (elementwise.cu)
+cudaError_t launch_rmsnorm(uint16_t* res_out, uint16_t* y, float* rstd, float* stats,
+                           const uint16_t* res_in, const uint16_t* x, const uint16_t* gain,
+                           float eps, int64_t N, int C, cudaStream_t s);
+cudaError_t launch_absmax(float* stats, const uint16_t* in, int64_t n, cudaStream_t s);
+cudaError_t launch_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t n,
+                            cudaStream_t s);
+cudaError_t launch_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, int64_t rows,
+                                 int cols, cudaStream_t s);
+// SwiGLU over gate_up [N, 2H]: writes h (if non-NULL) and max|h| into stats[0]
+// (zeroed first).
+cudaError_t launch_swiglu_absmax(uint16_t* h, float* stats, const uint16_t* gate_up, int64_t N,
+                                 int64_t H, cudaStream_t s);
+// Recomputes h from gate_up and quantises it with stats[0]; writes stats[1].
+cudaError_t launch_swiglu_requant(uint8_t* hq, float* stats, const uint16_t* gate_up, int64_t N,
+                                  int64_t H, cudaStream_t s);
+cudaError_t launch_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, bool pdl, cudaStream_t s);
+
+// ---- tcgen05 FP8 GEMMs (gemm_fp8.cu)
+// out[M,N] = bf16(a_scale*w_scale * A[M,K] . W[N,K]^T)
+cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
+                             const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
+                             int64_t K, cudaStream_t s);
+// h[M,H] = bf16(silu(g)*u) with g, u the bf16-rounded gate / up products of
+// W1 = [2H, K]; records max|h| into stats_h[0] (zeroed first).
+cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, const float* a_scale,
+                               const uint8_t* W1, const float* w_scale, int64_t M, int64_t H,
+                               int64_t K, cudaStream_t s);
+// Reads and clears the GEMM kernels' device status word of the current device.
+cudaError_t gemm_take_status(unsigned int* status);
+
+// ---- decode GEMVs (decode.cu)
+// out0[r] = bf16(s0[r] * W0[r,:] . x); with W1 != NULL also out1 from W1, s1.
+cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const uint8_t* w0,
+                        const float* s0, const uint8_t* w1, const float* s1, int64_t rows,
+                        int64_t cols, bool pdl, cudaStream_t s);
+
+}  // namespace qffn
