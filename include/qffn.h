@@ -27,8 +27,10 @@
  *    finite E4M3); codes are e4m3(x * (448 / abs_max)) with the product in
  *    fp32, rounded to nearest even and saturated to +-448.  abs_max == 0 gives
  *    scale 1 and all-zero codes.
- *  - Device pointers must be 16-byte aligned (QFFN_ERR_MISALIGNED otherwise);
- *    required pointers must be non-NULL (QFFN_ERR_INVALID_ARG).
+ *  - bf16 and E4M3 tensors must start on a 16-byte boundary, fp32 pointers
+ *    (stats pairs, scales, rstd, row scales) on a 4-byte boundary
+ *    (QFFN_ERR_MISALIGNED otherwise); required pointers must be non-NULL
+ *    (QFFN_ERR_INVALID_ARG).
  *  - Arguments are checked on the host before anything is enqueued; on any
  *    error nothing is enqueued.  Work is enqueued asynchronously on `stream`
  *    (NULL = the legacy default stream) and the call returns without waiting.
@@ -55,7 +57,7 @@ typedef enum qffn_status {
   QFFN_OK = 0,
   QFFN_ERR_INVALID_ARG = 1,       /* NULL pointer, negative size, bad eps, small workspace */
   QFFN_ERR_UNSUPPORTED_SHAPE = 2, /* a size outside the rules stated per call */
-  QFFN_ERR_MISALIGNED = 3,        /* a pointer not 16-byte aligned */
+  QFFN_ERR_MISALIGNED = 3,        /* a pointer below its required alignment */
   QFFN_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
   QFFN_ERR_TIMEOUT = 5            /* a device-side bounded wait ran out */
 } qffn_status;

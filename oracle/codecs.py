@@ -27,6 +27,21 @@ import numpy as np
 
 E4M3_MAX = 448.0
 
+# Element-wise conversions of large arrays run over flat slices of this many
+# elements, only to bound the size of the float64 temporaries.
+_CHUNK = 1 << 22
+
+
+def _chunked(fn, x, out_dtype):
+    x = np.asarray(x)
+    if x.size <= _CHUNK:
+        return fn(x)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=out_dtype)
+    for i in range(0, flat.size, _CHUNK):
+        out[i:i + _CHUNK] = fn(flat[i:i + _CHUNK])
+    return out.reshape(x.shape)
+
 
 # --------------------------------------------------------------------- bf16
 def bf16_to_f64(bits) -> np.ndarray:
@@ -42,6 +57,11 @@ def bf16_to_f32(bits) -> np.ndarray:
 
 
 def f64_to_bf16(x) -> np.ndarray:
+    """Round float64 values to bf16 (nearest, ties to even), one rounding."""
+    return _chunked(_f64_to_bf16, x, np.uint16)
+
+
+def _f64_to_bf16(x) -> np.ndarray:
     """Round float64 values to bf16 (nearest, ties to even), one rounding.
 
     A bf16 normal number has 8 significant bits, so in the binade
@@ -66,8 +86,8 @@ def f32_to_bf16(x) -> np.ndarray:
 
 
 # --------------------------------------------------------------------- e4m3
-def e4m3_decode(codes) -> np.ndarray:
-    """E4M3 bit patterns (uint8) -> exact float64 values (NaN for 0x7F/0xFF)."""
+def _e4m3_field_value(codes) -> np.ndarray:
+    """E4M3 bit patterns -> exact float64 values, from the sign/exponent/mantissa fields."""
     c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
     s = (c >> 7) & 1
     e = (c >> 3) & 0xF
@@ -77,6 +97,15 @@ def e4m3_decode(codes) -> np.ndarray:
                    np.ldexp((8 + m).astype(np.float64), e - 10))
     mag = np.where((e == 15) & (m == 7), np.nan, mag)
     return np.where(s == 1, -mag, mag)
+
+
+# value of every one of the 256 codes, by the field definition above
+_E4M3_VALUES = _e4m3_field_value(np.arange(256, dtype=np.uint8))
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 bit patterns (uint8) -> exact float64 values (NaN for 0x7F/0xFF)."""
+    return _E4M3_VALUES[np.asarray(codes, dtype=np.uint8)]
 
 
 def e4m3_to_scaled_int(codes) -> np.ndarray:
@@ -89,6 +118,11 @@ def e4m3_to_scaled_int(codes) -> np.ndarray:
 
 
 def e4m3_encode(v) -> np.ndarray:
+    """Round float values to E4M3 codes: nearest, ties to even, satfinite."""
+    return _chunked(_e4m3_encode, v, np.uint8)
+
+
+def _e4m3_encode(v) -> np.ndarray:
     """Round float values to E4M3 codes: nearest, ties to even, satfinite.
 
     For ``|v|`` in the binade ``[2**E, 2**(E+1))`` with ``E >= -6`` the

@@ -1,0 +1,200 @@
+"""End-to-end GPU parity of qffn_forward (the whole prefill chain A1..A5).
+
+Small and medium workloads are compared with the oracle over every element;
+the Qwen2.5-7B-shaped and Llama-3-8B workloads run at full size and are
+checked on sampled rows stage by stage (each stage fed the GPU's own
+upstream tensor) plus whole-tensor properties computed on the device.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ffn_inputs import PREFILL, PrefillConfig, prefill_inputs
+from gpu_util import assert_out_close, bf, bf16_ulp_diff, dev, e4m3_step_diff, empty_bf16, host, sync
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    import transformer_ffn_block_gb300 as q
+    return q
+
+
+def _gpu_weight_record(q, w_bits):
+    """Per-tensor E4M3 record built on the GPU (qffn_absmax + qffn_quantize)."""
+    wd = dev(w_bits)
+    stats = torch.zeros(2, dtype=torch.float32, device="cuda")
+    codes = torch.empty(w_bits.shape, dtype=torch.uint8, device="cuda")
+    q.qffn_absmax(stats, wd, w_bits.size)
+    q.qffn_quantize(codes, stats, wd, w_bits.size)
+    return codes, stats
+
+
+def run_forward(q, cfg, inp, with_res=True):
+    N, C, H = cfg.N, cfg.C, cfg.H
+    w1, s1 = _gpu_weight_record(q, inp["w1"])
+    w2, s2 = _gpu_weight_record(q, inp["w2"])
+    res_out = empty_bf16(N, C) if with_res else None
+    out = empty_bf16(N, C)
+    rstd = torch.empty(N, dtype=torch.float32, device="cuda")
+    stats = torch.full((4,), -1.0, dtype=torch.float32, device="cuda")
+    ws_bytes = q.qffn_forward_workspace_size(cfg.B, cfg.T, C, H)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    q.qffn_forward(res_out, out, rstd, stats[0:2], stats[2:4], dev(inp["res"]) if with_res else None,
+                   dev(inp["x"]), dev(inp["gain"]), inp["eps"], w1, s1[1:2], w2, s2[1:2],
+                   cfg.B, cfg.T, C, H, ws)
+    q.qffn_check_status()
+    sync()
+    off = q.qffn_forward_workspace_offsets(cfg.B, cfg.T, C, H)
+    y = ws[off[0]:off[0] + N * C * 2].view(torch.int16).view(N, C)
+    yq = ws[off[1]:off[1] + N * C].view(N, C)
+    h = ws[off[2]:off[2] + N * H * 2].view(torch.int16).view(N, H)
+    hq = ws[off[3]:off[3] + N * H].view(N, H)
+    return dict(res_out=res_out, out=out, rstd=rstd, stats=stats, y=y, yq=yq, h=h, hq=hq,
+                w1=w1, s1=s1, w2=w2, s2=s2)
+
+
+def check_full(q, cfg, with_res=True):
+    inp = prefill_inputs(cfg)
+    g = run_forward(q, cfg, inp, with_res)
+    w1q, w1s = oracle.quantize_tensor(inp["w1"])
+    w2q, w2s = oracle.quantize_tensor(inp["w2"])
+    # the GPU builds the same weight records bit for bit
+    np.testing.assert_array_equal(host(g["w1"]), w1q)
+    np.testing.assert_array_equal(host(g["w2"]), w2q)
+    assert host(g["s1"])[1] == w1s and host(g["s2"])[1] == w2s
+    ref = oracle.ffn_forward(inp["res"] if with_res else None, inp["x"], inp["gain"], inp["eps"],
+                             w1q, w1s, w2q, w2s, cfg.H)
+    st = host(g["stats"])
+    y, yq, h, hq = bf(g["y"]), host(g["yq"]), bf(g["h"]), host(g["hq"])
+
+    # A1
+    if with_res:
+        np.testing.assert_array_equal(bf(g["res_out"]), ref["r"])
+    d = bf16_ulp_diff(y, ref["y"])
+    assert d.max() <= 1 and (d > 0).mean() <= 1e-3
+    np.testing.assert_allclose(host(g["rstd"]), ref["rstd"], rtol=2e-6)
+    assert st[0] == np.float32(np.max(np.abs(oracle.bf16_to_f64(y))))          # abs-max bit-exact
+    # A2: stage-wise bit-exact codes and scale; end to end <= 0.1% codes off by one step
+    codes, scale = oracle.quantize_with_abs_max(y, st[0])
+    np.testing.assert_array_equal(yq, codes)
+    assert st[1] == scale
+    dq = e4m3_step_diff(yq, ref["yq"])
+    assert dq.max() <= 1 and (dq > 0).mean() <= 1e-3
+    # A3+A4: h from the GPU's own yq
+    h_stage, _ = oracle.swiglu(oracle.fp8_gemm_scaled(yq, st[1], w1q, w1s), cfg.H)
+    dh = bf16_ulp_diff(h, h_stage)
+    assert (dh > 0).mean() <= 2e-3
+    assert_out_close(h, h_stage, rel_l2=1e-3, max_abs_rms=1e-2)
+    assert st[2] == np.float32(np.max(np.abs(oracle.bf16_to_f64(h))))
+    codes, scale = oracle.quantize_with_abs_max(h, st[2])
+    np.testing.assert_array_equal(hq, codes)
+    assert st[3] == scale
+    dq = e4m3_step_diff(hq, ref["hq"])
+    assert (dq > 0).mean() <= 2e-3
+    # A5 from the GPU's own hq
+    out = bf(g["out"])
+    out_stage = oracle.fp8_gemm_scaled(hq, st[3], w2q, w2s)
+    assert (out != out_stage).mean() <= 2e-3
+    assert_out_close(out, out_stage, rel_l2=1e-3, max_abs_rms=1e-2)
+    # the acceptance rule against the end-to-end oracle
+    return assert_out_close(out, ref["out"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3.2-1b"])
+def test_forward_full_parity(q, name):
+    check_full(q, PREFILL[name])
+
+
+def test_forward_qwen_outliers_full_parity(q):
+    """Qwen2.5-7B shape, 0.1% outliers x20: stresses the abs-max scaling end to end."""
+    check_full(q, PREFILL["qwen2.5-7b"])
+
+
+@pytest.mark.parametrize("B,T,C,H", [(1, 1, 128, 128), (3, 43, 256, 384), (1, 129, 384, 512),
+                                     (2, 200, 1024, 2816)])
+def test_forward_ragged_shapes(q, B, T, C, H):
+    check_full(q, PrefillConfig("ragged", B=B, T=T, C=C, H=H, eps=1e-5, seed=B * T + C))
+
+
+def test_forward_without_residual(q):
+    check_full(q, PREFILL["tiny"], with_res=False)
+
+
+def test_forward_zero_input(q):
+    cfg = PrefillConfig("zeros", B=1, T=70, C=256, H=256, eps=1e-5)
+    inp = prefill_inputs(cfg)
+    inp["res"][:] = 0
+    inp["x"][:] = 0
+    g = run_forward(q, cfg, inp)
+    st = host(g["stats"])
+    assert st.tolist() == [0.0, 1.0, 0.0, 1.0]
+    assert not host(g["yq"]).any() and not host(g["hq"]).any()
+    assert not np.any(oracle.bf16_to_f64(bf(g["out"])))
+
+
+def test_forward_empty(q):
+    cfg = PrefillConfig("empty", B=0, T=16, C=256, H=256, eps=1e-5)
+    stats = torch.full((4,), 3.0, dtype=torch.float32, device="cuda")
+    w = torch.zeros(2 * 256 * 256, dtype=torch.uint8, device="cuda")
+    sc = torch.ones(2, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(q.qffn_forward_workspace_size(0, 16, 256, 256), 256), dtype=torch.uint8, device="cuda")
+    dummy = empty_bf16(8)
+    q.qffn_forward(dummy, dummy, sc, stats[0:2], stats[2:4], dummy, dummy, dummy, 1e-5, w, sc[0:1],
+                   w, sc[1:2], 0, 16, 256, 256, ws)
+    sync()
+    assert host(stats)[[0, 2]].tolist() == [0.0, 0.0]
+
+
+def test_forward_repeatable(q):
+    """Two calls on the same inputs give identical bits (stats re-zeroed each call)."""
+    cfg = PREFILL["tiny"]
+    inp = prefill_inputs(cfg)
+    a = run_forward(q, cfg, inp)
+    b = run_forward(q, cfg, inp)
+    for k in ("out", "res_out", "h", "hq", "stats"):
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_forward_llama3_8b_sampled(q):
+    """Full Llama-3-8B shape (N=16384, C=4096, H=14336) in the launch configuration the
+    benchmark times; sampled rows checked stage by stage, whole tensors by properties."""
+    cfg = PREFILL["llama3-8b"]
+    inp = prefill_inputs(cfg)
+    g = run_forward(q, cfg, inp)
+    N = cfg.N
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 8191, N - 2, N - 1],
+                                     np.random.default_rng(0).integers(0, N, 57)]))
+    st = host(g["stats"])
+    # whole-tensor abs-max properties (on the device)
+    assert st[0] == torch.max(torch.abs(g["y"].view(torch.bfloat16).float())).item()
+    assert st[2] == torch.max(torch.abs(g["h"].view(torch.bfloat16).float())).item()
+    assert st[1] == np.float32(st[0] / np.float32(448)) and st[3] == np.float32(st[2] / np.float32(448))
+    w1q, w1s = oracle.quantize_tensor(inp["w1"])
+    w2q, w2s = oracle.quantize_tensor(inp["w2"])
+    np.testing.assert_array_equal(host(g["w1"]), w1q)
+    np.testing.assert_array_equal(host(g["w2"]), w2q)
+    r, y_ref, rstd_ref, _ = oracle.residual_rmsnorm_absmax(inp["res"][rows], inp["x"][rows], inp["gain"], inp["eps"])
+    np.testing.assert_array_equal(bf(g["res_out"])[rows], r)
+    y = bf(g["y"])[rows]
+    assert bf16_ulp_diff(y, y_ref).max() <= 1
+    np.testing.assert_allclose(host(g["rstd"])[rows], rstd_ref, rtol=2e-6)
+    yq = host(g["yq"])[rows]
+    np.testing.assert_array_equal(yq, oracle.quantize_with_abs_max(y, st[0])[0])
+    h = bf(g["h"])[rows]
+    h_stage, _ = oracle.swiglu(oracle.fp8_gemm_scaled(yq, st[1], w1q, w1s), cfg.H)
+    assert (bf16_ulp_diff(h, h_stage) > 0).mean() <= 2e-3
+    assert_out_close(h, h_stage, rel_l2=1e-3, max_abs_rms=1e-2)
+    hq = host(g["hq"])[rows]
+    np.testing.assert_array_equal(hq, oracle.quantize_with_abs_max(h, st[2])[0])
+    out = bf(g["out"])[rows]
+    out_stage = oracle.fp8_gemm_scaled(hq, st[3], w2q, w2s)
+    assert (out != out_stage).mean() <= 2e-3
+    assert_out_close(out, out_stage, rel_l2=1e-3, max_abs_rms=1e-2)
+    # end to end on the sampled rows, the oracle chain using the oracle's own y rows
+    yq_ref = oracle.quantize_with_abs_max(y_ref, st[0])[0]
+    h_ref, _ = oracle.swiglu(oracle.fp8_gemm_scaled(yq_ref, st[1], w1q, w1s), cfg.H)
+    out_ref = oracle.fp8_gemm_scaled(oracle.quantize_with_abs_max(h_ref, st[2])[0], st[3], w2q, w2s)
+    assert_out_close(out, out_ref)

@@ -24,6 +24,8 @@ inline qffn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QFFN_OK 
   } while (0)
 #define QFFN_PTR(p) QFFN_REQUIRE((p) != nullptr, QFFN_ERR_INVALID_ARG)
 #define QFFN_ALIGNED(p) QFFN_REQUIRE((p) == nullptr || aligned16(p), QFFN_ERR_MISALIGNED)
+// fp32 scalars and vectors (stats pairs, scales, rstd, row scales): natural alignment
+#define QFFN_ALIGNED4(p) QFFN_REQUIRE((reinterpret_cast<uintptr_t>(p) & 3u) == 0, QFFN_ERR_MISALIGNED)
 #define QFFN_CUDA(expr)                              \
   do {                                               \
     cudaError_t e_ = (expr);                         \
@@ -59,7 +61,7 @@ const char* qffn_status_string(qffn_status s) {
     case QFFN_OK: return "ok";
     case QFFN_ERR_INVALID_ARG: return "invalid argument";
     case QFFN_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
-    case QFFN_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case QFFN_ERR_MISALIGNED: return "misaligned pointer";
     case QFFN_ERR_CUDA: return "CUDA error";
     case QFFN_ERR_TIMEOUT: return "device-side wait timed out";
   }
@@ -84,9 +86,9 @@ qffn_status qffn_rmsnorm_absmax(uint16_t* res_out, uint16_t* y, float* rstd, flo
   QFFN_REQUIRE(isfinite(eps) && eps >= 0.0f, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
   QFFN_REQUIRE(C % 8 == 0 && C >= 8 && C <= 16384, QFFN_ERR_UNSUPPORTED_SHAPE);
-  QFFN_ALIGNED(y); QFFN_ALIGNED(x); QFFN_ALIGNED(gain); QFFN_ALIGNED(rstd);
+  QFFN_ALIGNED(y); QFFN_ALIGNED(x); QFFN_ALIGNED(gain); QFFN_ALIGNED4(rstd);
   if (res_in != nullptr) { QFFN_ALIGNED(res_in); QFFN_ALIGNED(res_out); }
-  QFFN_REQUIRE(stats == nullptr || aligned16(stats), QFFN_ERR_MISALIGNED);
+  QFFN_ALIGNED4(stats);
   return from_cuda(qffn::launch_rmsnorm(res_out, y, rstd, stats, res_in, x, gain, eps, N, int(C),
                                         stream));
 }
@@ -94,7 +96,7 @@ qffn_status qffn_rmsnorm_absmax(uint16_t* res_out, uint16_t* y, float* rstd, flo
 qffn_status qffn_absmax(float* stats, const uint16_t* in, int64_t n, qffn_stream_t stream) {
   QFFN_PTR(stats); QFFN_PTR(in);
   QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);
-  QFFN_ALIGNED(stats); QFFN_ALIGNED(in);
+  QFFN_ALIGNED4(stats); QFFN_ALIGNED(in);
   return from_cuda(qffn::launch_absmax(stats, in, n, stream));
 }
 
@@ -102,7 +104,7 @@ qffn_status qffn_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t 
                           qffn_stream_t stream) {
   QFFN_PTR(q); QFFN_PTR(stats); QFFN_PTR(in);
   QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);
-  QFFN_ALIGNED(q); QFFN_ALIGNED(stats); QFFN_ALIGNED(in);
+  QFFN_ALIGNED(q); QFFN_ALIGNED4(stats); QFFN_ALIGNED(in);
   return from_cuda(qffn::launch_quantize(q, stats, in, n, stream));
 }
 
@@ -112,7 +114,7 @@ qffn_status qffn_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, 
   QFFN_REQUIRE(rows >= 0 && cols >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(rows <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
   QFFN_REQUIRE(cols % 16 == 0 && cols >= 16 && cols <= 65536, QFFN_ERR_UNSUPPORTED_SHAPE);
-  QFFN_ALIGNED(q); QFFN_ALIGNED(row_scale); QFFN_ALIGNED(w);
+  QFFN_ALIGNED(q); QFFN_ALIGNED4(row_scale); QFFN_ALIGNED(w);
   return from_cuda(qffn::launch_quantize_rows(q, row_scale, w, rows, int(cols), stream));
 }
 
@@ -125,7 +127,7 @@ qffn_status qffn_fp8_gemm_scaled(uint16_t* out, const uint8_t* A, const float* a
   QFFN_REQUIRE(N % 32 == 0 && N >= 32 && N <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
   QFFN_REQUIRE(K % 16 == 0 && K >= 16 && K <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
   QFFN_REQUIRE((M + 127) / 128 * ((N + 255) / 256) < (int64_t(1) << 31), QFFN_ERR_UNSUPPORTED_SHAPE);
-  QFFN_ALIGNED(out); QFFN_ALIGNED(A); QFFN_ALIGNED(W);
+  QFFN_ALIGNED(out); QFFN_ALIGNED(A); QFFN_ALIGNED(W); QFFN_ALIGNED4(a_scale); QFFN_ALIGNED4(w_scale);
   return from_cuda(qffn::launch_gemm_bf16(out, A, a_scale, W, w_scale, M, N, K, stream));
 }
 
@@ -138,7 +140,8 @@ qffn_status qffn_gate_up_swiglu(uint16_t* h, float* stats_h, const uint8_t* yq,
   QFFN_REQUIRE(C % 16 == 0 && C >= 16 && C <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
   QFFN_REQUIRE(H % 128 == 0 && H >= 128 && H <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
   QFFN_REQUIRE((N + 127) / 128 * (H / 128) < (int64_t(1) << 31), QFFN_ERR_UNSUPPORTED_SHAPE);
-  QFFN_ALIGNED(h); QFFN_ALIGNED(stats_h); QFFN_ALIGNED(yq); QFFN_ALIGNED(w1);
+  QFFN_ALIGNED(h); QFFN_ALIGNED4(stats_h); QFFN_ALIGNED(yq); QFFN_ALIGNED(w1);
+  QFFN_ALIGNED4(y_scale); QFFN_ALIGNED4(w1_scale);
   return from_cuda(qffn::launch_gemm_swiglu(h, stats_h, yq, y_scale, w1, w1_scale, N, H, C, stream));
 }
 
@@ -147,7 +150,7 @@ qffn_status qffn_swiglu_quant(uint16_t* h, uint8_t* hq, float* stats, const uint
   QFFN_PTR(hq); QFFN_PTR(stats); QFFN_PTR(gate_up);
   QFFN_REQUIRE(N >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(H % 8 == 0 && H >= 8 && H <= kMaxDim && N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
-  QFFN_ALIGNED(h); QFFN_ALIGNED(hq); QFFN_ALIGNED(stats); QFFN_ALIGNED(gate_up);
+  QFFN_ALIGNED(h); QFFN_ALIGNED(hq); QFFN_ALIGNED4(stats); QFFN_ALIGNED(gate_up);
   QFFN_CUDA(qffn::launch_swiglu_absmax(h, stats, gate_up, N, H, stream));
   if (h != nullptr) return from_cuda(qffn::launch_quantize(hq, stats, h, N * H, stream));
   return from_cuda(qffn::launch_swiglu_requant(hq, stats, gate_up, N, H, stream));
@@ -189,8 +192,9 @@ qffn_status qffn_forward(uint16_t* res_out, uint16_t* out, float* rstd, float* s
   forward_offsets(N, C, H, off);
   QFFN_REQUIRE(workspace_bytes >= off[4], QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(aligned256(workspace), QFFN_ERR_MISALIGNED);
-  QFFN_ALIGNED(out); QFFN_ALIGNED(rstd); QFFN_ALIGNED(stats_y); QFFN_ALIGNED(stats_h);
+  QFFN_ALIGNED(out); QFFN_ALIGNED4(rstd); QFFN_ALIGNED4(stats_y); QFFN_ALIGNED4(stats_h);
   QFFN_ALIGNED(x); QFFN_ALIGNED(gain); QFFN_ALIGNED(w1); QFFN_ALIGNED(w2);
+  QFFN_ALIGNED4(w1_scale); QFFN_ALIGNED4(w2_scale);
   if (res_in != nullptr) { QFFN_ALIGNED(res_in); QFFN_ALIGNED(res_out); }
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -217,7 +221,7 @@ qffn_status qffn_gemv_dual(uint16_t* g, uint16_t* u, const uint16_t* x, const ui
   QFFN_PTR(g); QFFN_PTR(u); QFFN_PTR(x); QFFN_PTR(w_gate); QFFN_PTR(s_gate); QFFN_PTR(w_up); QFFN_PTR(s_up);
   QFFN_REQUIRE(H >= 1 && C >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(C % 16 == 0 && C >= 16 && C <= 32768 && H <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
-  QFFN_ALIGNED(x); QFFN_ALIGNED(w_gate); QFFN_ALIGNED(w_up);
+  QFFN_ALIGNED(x); QFFN_ALIGNED(w_gate); QFFN_ALIGNED(w_up); QFFN_ALIGNED4(s_gate); QFFN_ALIGNED4(s_up);
   return from_cuda(qffn::launch_gemv(g, u, x, w_gate, s_gate, w_up, s_up, H, C, false, stream));
 }
 
@@ -227,7 +231,7 @@ qffn_status qffn_gemv(uint16_t* out, const uint16_t* x, const uint8_t* w, const 
   QFFN_REQUIRE(rows >= 1 && cols >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(cols % 16 == 0 && cols >= 16 && cols <= 32768 && rows <= kMaxRows,
                QFFN_ERR_UNSUPPORTED_SHAPE);
-  QFFN_ALIGNED(x); QFFN_ALIGNED(w);
+  QFFN_ALIGNED(x); QFFN_ALIGNED(w); QFFN_ALIGNED4(row_scale);
   return from_cuda(qffn::launch_gemv(out, nullptr, x, w, row_scale, nullptr, nullptr, rows, cols,
                                      false, stream));
 }
@@ -255,6 +259,7 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
                QFFN_ERR_UNSUPPORTED_SHAPE);
   QFFN_REQUIRE(workspace_bytes >= qffn_decode_workspace_size(C, H), QFFN_ERR_INVALID_ARG);
   QFFN_ALIGNED(out); QFFN_ALIGNED(x); QFFN_ALIGNED(w_gate); QFFN_ALIGNED(w_up); QFFN_ALIGNED(w_down);
+  QFFN_ALIGNED4(s_gate); QFFN_ALIGNED4(s_up); QFFN_ALIGNED4(s_down);
   QFFN_ALIGNED(workspace);
   uint16_t* g = static_cast<uint16_t*>(workspace);
   uint16_t* u = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + round_up(size_t(H) * 2, 256));
