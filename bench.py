@@ -463,6 +463,38 @@ def run_reference(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def profile_case(q, torch, device):
+    """A case sized for ncu captures: the prefill chain at N=4096 tokens of the 8B FFN
+    (C=4096, H=14336; ~1.3 GB on the device, larger than L2) three times, then the
+    8B decode FFN twice.  Launch order per forward: rmsnorm, quantize, gate|up GEMM,
+    quantize, down GEMM."""
+    global PREFILL_CFG
+    from ffn_inputs import PrefillConfig
+    PREFILL_CFG = PrefillConfig("llama3-8b-4k", B=2, T=2048, C=4096, H=14336, eps=1e-5)
+    d = prefill_setup(q, torch, device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(3):
+        forward(q, d, stream)
+    torch.cuda.synchronize()
+    q.qffn_check_status(stream)
+    cfg = DECODE_CFG
+    di = decode_inputs(cfg)
+    recs = []
+    for k, rows, cols in (("w_gate", cfg.H, cfg.C), ("w_up", cfg.H, cfg.C), ("w_down", cfg.C, cfg.H)):
+        wb = to_dev(di[k], torch, device)
+        codes = torch.empty(rows, cols, dtype=torch.uint8, device=device)
+        sc = torch.empty(rows, dtype=torch.float32, device=device)
+        q.qffn_quantize_rows(codes, sc, wb, rows, cols)
+        recs += [codes, sc]
+    x = to_dev(di["x"], torch, device)
+    out = torch.empty(cfg.C, dtype=torch.int16, device=device)
+    ws = torch.empty(q.qffn_decode_workspace_size(cfg.C, cfg.H), dtype=torch.uint8, device=device)
+    for _ in range(2):
+        q.qffn_decode_forward(out, x, *recs, cfg.C, cfg.H, ws, stream=stream)
+    torch.cuda.synchronize()
+    print("profile case done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -471,6 +503,8 @@ def main():
     ap.add_argument("--impl", default="qffn", choices=["qffn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-iters", type=int, default=300)
+    ap.add_argument("--profile-case", action="store_true",
+                    help="run a small case once (for ncu captures) and exit without timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -483,6 +517,9 @@ def main():
     import transformer_ffn_block_gb300 as q
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.profile_case:
+        profile_case(q, torch, device)
+        return
     peaks = load_peaks()
     pre = bench_prefill(q, torch, device, args.steps, args.warmup, dist, peaks)
     dec = bench_decode(q, torch, device, args.decode_iters, dist, peaks)

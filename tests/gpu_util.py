@@ -75,3 +75,19 @@ def assert_out_close(got_bits, want_bits, rel_l2=1e-2, max_abs_rms=5e-2):
 
 def sync():
     torch.cuda.synchronize()
+
+
+def check_dot_outputs(got_bits, want_bits, absdot, K, max_mismatch):
+    """Outputs of fp32-accumulated dot products against the exact-then-rounded values:
+    |got - want| <= 1 bf16 ulp + K * 2**-22 * absdot (absdot = scale * sum|terms|), and at
+    most `max_mismatch` of the outputs differ at all."""
+    g = oracle.bf16_to_f64(got_bits)
+    w = oracle.bf16_to_f64(want_bits)
+    big = np.maximum(np.abs(g), np.abs(w))
+    ulp = np.ldexp(1.0, np.frexp(np.maximum(big, 1e-30))[1] - 8)
+    bound = ulp + K * 2.0 ** -22 * absdot
+    err = np.abs(g - w)
+    frac = float(np.mean(got_bits != want_bits))
+    assert np.all(err <= bound), (float(np.max(err / bound)), frac)
+    assert frac <= max_mismatch, frac
+    return frac

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 from ffn_inputs import DECODE, DecodeConfig, decode_inputs
-from gpu_util import assert_out_close, bf, bf16_ulp_diff, dev, empty_bf16, host, sync
+from gpu_util import assert_out_close, bf, bf16_ulp_diff, check_dot_outputs, dev, empty_bf16, host, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -51,14 +51,16 @@ def test_decode_forward(q, C, H):
     q.qffn_gemv_dual(g, u, x, *recs["w_gate"], *recs["w_up"], cfg.H, cfg.C)
     sync()
     gb, ub = bf(g), bf(u)
-    for got, want in ((gb, ref["g"]), (ub, ref["u"])):
-        d = bf16_ulp_diff(got, want)
-        assert d.max() <= 2 and (d > 0).mean() <= 0.02
+    xa = np.abs(oracle.bf16_to_f64(di["x"]))
+    for got, want, (wq, ws_) in ((gb, ref["g"], ref_rec["w_gate"]), (ub, ref["u"], ref_rec["w_up"])):
+        absdot = (np.abs(oracle.e4m3_decode(wq)) @ xa) * ws_.astype(np.float64)
+        check_dot_outputs(got, want, absdot, cfg.C, max_mismatch=0.02)
     h_gpu = bf(ws[:2 * cfg.H].view(torch.int16))
     assert bf16_ulp_diff(h_gpu, oracle.silu_mul(gb, ub)).max() <= 1
     out_stage = oracle.gemv_row_scaled(h_gpu, *ref_rec["w_down"])
-    d = bf16_ulp_diff(bf(out), out_stage)
-    assert d.max() <= 2 and (d > 0).mean() <= 0.02
+    absdot = (np.abs(oracle.e4m3_decode(ref_rec["w_down"][0])) @ np.abs(oracle.bf16_to_f64(h_gpu))) \
+        * ref_rec["w_down"][1].astype(np.float64)
+    check_dot_outputs(bf(out), out_stage, absdot, cfg.H, max_mismatch=0.02)
 
 
 def test_decode_per_projection_arm_bit_identical(q):

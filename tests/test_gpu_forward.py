@@ -87,7 +87,7 @@ def check_full(q, cfg, with_res=True):
     h_stage, _ = oracle.swiglu(oracle.fp8_gemm_scaled(yq, st[1], w1q, w1s), cfg.H)
     dh = bf16_ulp_diff(h, h_stage)
     assert (dh > 0).mean() <= 2e-3
-    assert_out_close(h, h_stage, rel_l2=1e-3, max_abs_rms=1e-2)
+    assert_out_close(h, h_stage, rel_l2=1e-3)
     assert st[2] == np.float32(np.max(np.abs(oracle.bf16_to_f64(h))))
     codes, scale = oracle.quantize_with_abs_max(h, st[2])
     np.testing.assert_array_equal(hq, codes)
@@ -98,7 +98,7 @@ def check_full(q, cfg, with_res=True):
     out = bf(g["out"])
     out_stage = oracle.fp8_gemm_scaled(hq, st[3], w2q, w2s)
     assert (out != out_stage).mean() <= 2e-3
-    assert_out_close(out, out_stage, rel_l2=1e-3, max_abs_rms=1e-2)
+    assert_out_close(out, out_stage, rel_l2=1e-3)
     # the acceptance rule against the end-to-end oracle
     return assert_out_close(out, ref["out"])
 
@@ -186,13 +186,13 @@ def test_forward_llama3_8b_sampled(q):
     h = bf(g["h"])[rows]
     h_stage, _ = oracle.swiglu(oracle.fp8_gemm_scaled(yq, st[1], w1q, w1s), cfg.H)
     assert (bf16_ulp_diff(h, h_stage) > 0).mean() <= 2e-3
-    assert_out_close(h, h_stage, rel_l2=1e-3, max_abs_rms=1e-2)
+    assert_out_close(h, h_stage, rel_l2=1e-3)
     hq = host(g["hq"])[rows]
     np.testing.assert_array_equal(hq, oracle.quantize_with_abs_max(h, st[2])[0])
     out = bf(g["out"])[rows]
     out_stage = oracle.fp8_gemm_scaled(hq, st[3], w2q, w2s)
     assert (out != out_stage).mean() <= 2e-3
-    assert_out_close(out, out_stage, rel_l2=1e-3, max_abs_rms=1e-2)
+    assert_out_close(out, out_stage, rel_l2=1e-3)
     # end to end on the sampled rows, the oracle chain using the oracle's own y rows
     yq_ref = oracle.quantize_with_abs_max(y_ref, st[0])[0]
     h_ref, _ = oracle.swiglu(oracle.fp8_gemm_scaled(yq_ref, st[1], w1q, w1s), cfg.H)
