@@ -464,14 +464,15 @@ def run_reference(args, rank, world, dist):
 
 
 def profile_case(q, torch, device):
-    """A case sized for ncu captures: the prefill chain at N=4096 tokens of the 8B FFN
-    (C=4096, H=14336; ~1.3 GB on the device, larger than L2) three times, then the
-    8B decode FFN twice.  Launch order per forward: rmsnorm, quantize, gate|up GEMM,
+    """A case sized for ncu captures: the prefill chain at N=2048 tokens of the 8B FFN
+    (C=4096, H=14336; weights alone 176 MB, larger than L2; under 1 GB on the device)
+    three times, then the 8B decode FFN twice.  Launch order per forward: rmsnorm, quantize, gate|up GEMM,
     quantize, down GEMM."""
     global PREFILL_CFG
     from ffn_inputs import PrefillConfig
-    PREFILL_CFG = PrefillConfig("llama3-8b-4k", B=2, T=2048, C=4096, H=14336, eps=1e-5)
+    PREFILL_CFG = PrefillConfig("llama3-8b-2k", B=1, T=2048, C=4096, H=14336, eps=1e-5)
     d = prefill_setup(q, torch, device)
+    torch.cuda.empty_cache()
     stream = torch.cuda.current_stream(device)
     for _ in range(3):
         forward(q, d, stream)
@@ -486,6 +487,9 @@ def profile_case(q, torch, device):
         sc = torch.empty(rows, dtype=torch.float32, device=device)
         q.qffn_quantize_rows(codes, sc, wb, rows, cols)
         recs += [codes, sc]
+    del wb
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     x = to_dev(di["x"], torch, device)
     out = torch.empty(cfg.C, dtype=torch.int16, device=device)
     ws = torch.empty(q.qffn_decode_workspace_size(cfg.C, cfg.H), dtype=torch.uint8, device=device)
