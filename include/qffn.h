@@ -195,6 +195,30 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
                                 const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
                                 void* workspace, size_t workspace_bytes, qffn_stream_t stream);
 
+/* ---- Decode FFN without a caller workspace ---------------------------------
+ * The pages have no counterpart of this call; it exists for callers that
+ * cannot allocate device memory (for example code running where cudaMalloc is
+ * not permitted, such as a plugin's enqueue step or a host callback, or a
+ * process whose device memory is all owned by another allocator) and so
+ * cannot supply the workspace of qffn_decode_forward.
+ * Computes exactly what qffn_decode_forward computes (same kernels, same
+ * bits), with the intermediate g and u vectors in a fixed scratch array
+ * inside the library: 2 x 32768 bf16 (128 KiB) per GPU that loads the
+ * library, held until the process exits.  H > 32768 is rejected with
+ * QFFN_ERR_UNSUPPORTED_SHAPE; the other size and alignment rules are those of
+ * qffn_decode_forward.  Nothing is allocated by this call.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls on a device share the array and it keeps the last call's
+ * contents (every element read is written first, so nothing needs
+ * clearing).  Calls that overlap in time on the GPU race on the array:
+ * order them on one stream or with events. */
+qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
+                                        const float* s_gate, const uint8_t* w_up,
+                                        const float* s_up, const uint8_t* w_down,
+                                        const float* s_down, int64_t C, int64_t H,
+                                        qffn_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

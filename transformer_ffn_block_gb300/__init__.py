@@ -22,7 +22,7 @@ __all__ = [
     "qffn_fp8_gemm_scaled", "qffn_gate_up_swiglu", "qffn_swiglu_quant",
     "qffn_forward_workspace_size", "qffn_forward_workspace_offsets", "qffn_forward",
     "qffn_gemv_dual", "qffn_gemv", "qffn_silu_mul", "qffn_decode_workspace_size",
-    "qffn_decode_forward",
+    "qffn_decode_forward", "qffn_decode_forward_noalloc",
 ]
 
 STATUS = {0: "QFFN_OK", 1: "QFFN_ERR_INVALID_ARG", 2: "QFFN_ERR_UNSUPPORTED_SHAPE",
@@ -61,6 +61,7 @@ _SIGS = {
     "qffn_silu_mul": ([_P, _P, _I64, _P], _S),
     "qffn_decode_workspace_size": ([_I64, _I64], _SZ),
     "qffn_decode_forward": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P], _S),
+    "qffn_decode_forward_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], _S),
 }
 for _name, (_args, _res) in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -192,3 +193,12 @@ def qffn_decode_forward(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H
     _check("qffn_decode_forward", lib.qffn_decode_forward(
         _ptr(out), _ptr(x), _ptr(w_gate), _ptr(s_gate), _ptr(w_up), _ptr(s_up), _ptr(w_down),
         _ptr(s_down), int(C), int(H), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def qffn_decode_forward_noalloc(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H,
+                                stream=None):
+    """qffn_decode_forward for callers that cannot allocate: the g/u scratch is a fixed
+    array inside the library (H <= 32768); calls overlapping on the GPU race on it."""
+    _check("qffn_decode_forward_noalloc", lib.qffn_decode_forward_noalloc(
+        _ptr(out), _ptr(x), _ptr(w_gate), _ptr(s_gate), _ptr(w_up), _ptr(s_up), _ptr(w_down),
+        _ptr(s_down), int(C), int(H), _stream(stream)))

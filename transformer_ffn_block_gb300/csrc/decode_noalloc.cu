@@ -1,0 +1,81 @@
+// Single-token decode FFN for callers that cannot allocate device memory.
+//
+// qffn_decode_forward needs a caller-provided workspace for the intermediate
+// gate and up vectors.  Some callers have no way to provide one: code that
+// runs where cudaMalloc is not allowed or not wanted (for example inside a
+// host callback, in a plugin whose enqueue step must not allocate, or in a
+// process whose device memory is entirely owned by another allocator) and
+// that cannot keep a buffer of its own around between calls.  This file gives
+// them an entry point whose scratch is a fixed array in the library's own
+// device memory instead.
+//
+// The scratch array below lives in every GPU that loads the library, for as
+// long as the process runs.  All calls on a device share it and it keeps what
+// the last call wrote; the decode writes every scratch element it reads
+// before reading it, so nothing needs clearing between calls.  Calls whose
+// execution overlaps on the GPU (different streams, no ordering between them)
+// use the same array and race; order them on one stream or with events.
+#include <mutex>
+
+#include "../../include/qffn.h"
+#include "launch.h"
+
+namespace {
+
+// Largest intermediate size H this entry point accepts: g and u, H bf16 each.
+constexpr int64_t kNoAllocMaxH = 32768;
+
+static __device__ __align__(256) uint16_t g_decode_scratch[2 * kNoAllocMaxH];
+
+// Device address of g_decode_scratch for each device, looked up once per
+// device with that device current.  In host code the array's name is only a
+// host-side stand-in, never a usable device address.
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {nullptr};
+
+cudaError_t scratch_address(uint16_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = static_cast<uint16_t*>(g_scratch_addr[dev]);
+  return cudaSuccess;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+}  // namespace
+
+extern "C" qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t* x,
+                                                   const uint8_t* w_gate, const float* s_gate,
+                                                   const uint8_t* w_up, const float* s_up,
+                                                   const uint8_t* w_down, const float* s_down,
+                                                   int64_t C, int64_t H, qffn_stream_t stream) {
+  if (!out || !x || !w_gate || !s_gate || !w_up || !s_up || !w_down || !s_down)
+    return QFFN_ERR_INVALID_ARG;
+  if (C % 16 != 0 || H % 16 != 0 || C < 16 || H < 16 || C > 32768 || H > kNoAllocMaxH)
+    return QFFN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(out) || !aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) ||
+      !aligned16(w_down) || !aligned4(s_gate) || !aligned4(s_up) || !aligned4(s_down))
+    return QFFN_ERR_MISALIGNED;
+  uint16_t* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return QFFN_ERR_CUDA;
+  uint16_t* g = scratch;
+  uint16_t* u = scratch + kNoAllocMaxH;
+  // the same three launches as qffn_decode_forward, with the scratch array as workspace
+  if (qffn::launch_gemv(g, u, x, w_gate, s_gate, w_up, s_up, H, C, false, stream) != cudaSuccess)
+    return QFFN_ERR_CUDA;
+  if (qffn::launch_silu_mul(g, u, H, true, stream) != cudaSuccess) return QFFN_ERR_CUDA;
+  if (qffn::launch_gemv(out, nullptr, g, w_down, s_down, nullptr, nullptr, C, H, true, stream) !=
+      cudaSuccess)
+    return QFFN_ERR_CUDA;
+  return QFFN_OK;
+}
