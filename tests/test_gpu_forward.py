@@ -93,16 +93,10 @@ def check_full(q, cfg, with_res=True):
     # A1
     if with_res:
         np.testing.assert_array_equal(bf(g["res_out"]), ref["r"])
-    d = bf16_ulp_diff(y, ref["y"])
-    assert d.max() <= 1 and (d > 0).mean() <= 1e-3
-    np.testing.assert_allclose(host(g["rstd"]), ref["rstd"], rtol=2e-6)
-    assert st[0] == np.float32(np.max(np.abs(oracle.bf16_to_f64(y))))          # abs-max bit-exact
-    # A2: stage-wise bit-exact codes and scale; end to end <= 0.1% codes off by one step
-    codes, scale = oracle.quantize_with_abs_max(y, st[0])
-    np.testing.assert_array_equal(yq, codes)
-    assert st[1] == scale
-    dq = e4m3_step_diff(yq, ref["yq"])
-    assert dq.max() <= 1 and (dq > 0).mean() <= 1e-3
+    np.testing.assert_array_equal(y, ref["y"])                                  # bit-exact
+    np.testing.assert_array_equal(host(g["rstd"]), ref["rstd"])
+    np.testing.assert_array_equal(st[0:2], ref["stats_y"])                     # abs-max, scale
+    np.testing.assert_array_equal(yq, ref["yq"])                               # codes
     # A3+A4 stage-wise: the fused h equals SwiGLU of the GPU's own unfused gate|up GEMM
     # of its own yq (within 1 ulp of the fp64 silu); that GEMM is within the fp32
     # accumulation bound of the exact product
@@ -196,8 +190,8 @@ def test_forward_llama3_8b_sampled(q):
     r, y_ref, rstd_ref, _ = oracle.residual_rmsnorm_absmax(inp["res"][rows], inp["x"][rows], inp["gain"], inp["eps"])
     np.testing.assert_array_equal(bf(g["res_out"])[rows], r)
     y = bf(g["y"])[rows]
-    assert bf16_ulp_diff(y, y_ref).max() <= 1
-    np.testing.assert_allclose(host(g["rstd"])[rows], rstd_ref, rtol=2e-6)
+    np.testing.assert_array_equal(y, y_ref)
+    np.testing.assert_array_equal(host(g["rstd"])[rows], rstd_ref)
     yq = host(g["yq"])[rows]
     np.testing.assert_array_equal(yq, oracle.quantize_with_abs_max(y, st[0])[0])
     h = bf(g["h"])[rows]

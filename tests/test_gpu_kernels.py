@@ -48,14 +48,11 @@ def test_rmsnorm_absmax(q, N, C, with_res):
     if with_res:
         np.testing.assert_array_equal(bf(res_out), r_ref)          # bit-exact
     yg = bf(y)
-    d = bf16_ulp_diff(yg, y_ref)
-    assert d.max() <= 1, d.max()
-    assert (d > 0).mean() <= 1e-3
-    np.testing.assert_allclose(host(rstd), rstd_ref, rtol=2e-6)
+    # y is rounded once from an almost exact value: bit-identical to the oracle
+    np.testing.assert_array_equal(yg, y_ref)
+    np.testing.assert_array_equal(host(rstd), rstd_ref)
     st = host(stats)
-    # abs-max is bit-exact with respect to the GPU's own y
-    assert st[0] == np.float32(np.max(np.abs(oracle.bf16_to_f64(yg))))
-    assert bf16_ulp_diff(oracle.f32_to_bf16(np.float32([st[0]])), oracle.f32_to_bf16(np.float32([amax_ref])))[0] <= 1
+    assert st[0] == amax_ref
     assert st[1] == 123.0                                           # scale slot untouched
 
 
@@ -71,7 +68,7 @@ def test_rmsnorm_in_place_and_no_stats(q):
     q.qffn_rmsnorm_absmax(xd, y, rstd, None, dev(res), xd, dev(gain), 1e-6, N, C)   # res_out aliases x
     sync()
     np.testing.assert_array_equal(bf(xd), r_ref)
-    assert bf16_ulp_diff(bf(y), y_ref).max() <= 1
+    np.testing.assert_array_equal(bf(y), y_ref)
 
 
 def test_rmsnorm_empty(q):

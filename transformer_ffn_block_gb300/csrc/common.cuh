@@ -50,6 +50,40 @@ QFFN_DEVI void e4m3x4_to_f32(uint32_t w, float& f0, float& f1, float& f2, float&
   f0 = fa.x; f1 = fa.y; f2 = fb.x; f3 = fb.y;
 }
 
+// ----------------------------------------------------------------- double-float
+// A value carried as an unevaluated sum hi + lo of two floats (about 48
+// significant bits).  two_sum is Knuth's error-free addition: s = fl(a + b)
+// and e = (a + b) - s exactly.
+QFFN_DEVI void two_sum(float a, float b, float& s, float& e) {
+  s = a + b;
+  const float bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+// (hi, lo) += x
+QFFN_DEVI void df_add(float& hi, float& lo, float x) {
+  float s, e;
+  two_sum(hi, x, s, e);
+  hi = s;
+  lo += e;
+}
+// (hi, lo) += (bhi, blo), renormalised so |lo| <= ulp(hi) / 2
+QFFN_DEVI void df_add_df(float& hi, float& lo, float bhi, float blo) {
+  float s, e;
+  two_sum(hi, bhi, s, e);
+  e += lo + blo;
+  hi = s + e;
+  lo = e - (hi - s);
+}
+// Round th + tl (|tl| <= ulp(th) / 2) to bf16, nearest-even, as one rounding:
+// th's own rounding decides unless th sits exactly halfway between two bf16
+// values, where the sign of tl (relative to th) picks the side.
+QFFN_DEVI uint32_t bf16_round_df(float th, float tl) {
+  const uint32_t bits = __float_as_uint(th);
+  uint32_t b = f32_to_bf16(th);
+  if ((bits & 0xFFFFu) == 0x8000u && tl != 0.0f) b = (bits >> 16) + (((tl > 0.0f) == (th > 0.0f)) ? 1u : 0u);
+  return b;
+}
+
 // ----------------------------------------------------------------- SwiGLU
 // silu(g) * u in fp32.  silu(g) = g * sigmoid(g); the sigmoid is formed from
 // e = exp(-|g|) in (0, 1] so neither branch overflows:

@@ -33,18 +33,26 @@ __device__ __forceinline__ float block_reduce_max(float v, float* red) {
 // One block of 128 threads per row; thread t owns the 16-byte chunks
 // t, t+128, ... of the row and keeps its residual sums in registers between
 // the sum-of-squares pass and the normalisation pass.
+//
+// y is rounded once from an almost exact value, so it agrees with the
+// correctly rounded r * rstd * g: each r^2 is exact in fp32 and is summed as
+// a double-float; mean, eps, sqrt and reciprocal are done once per row in
+// fp64 and rstd is split into a float pair (hi, lo); r * g is exact in fp32
+// and (r * g) * (hi + lo) is formed as a double-float with two fmas before
+// the single rounding to bf16.
 template <int V>
 __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_t* y, float* rstd,
                                                       float* stats, const uint16_t* res_in,
                                                       const uint16_t* x, const uint16_t* gain,
                                                       float eps, int C) {
-  __shared__ float red[4];
+  __shared__ float red[8];
+  __shared__ float s_rstd[2];
   const int64_t row = blockIdx.x;
   const int nchunk = C >> 3;
   const int tid = threadIdx.x;
   const size_t base = size_t(row) * size_t(C);
   uint4 rv[V];
-  float ss = 0.0f;
+  float ss_hi = 0.0f, ss_lo = 0.0f;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int c = tid + i * 128;
@@ -65,18 +73,35 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
-        ss = fmaf(lo, lo, ss);
-        ss = fmaf(hi, hi, ss);
+        df_add(ss_hi, ss_lo, lo * lo);     // squares of bf16 values are exact in fp32
+        df_add(ss_hi, ss_lo, hi * hi);
       }
     }
   }
-  // block sum of squares
-  ss = warp_sum(ss);
-  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  // block sum of squares (double-float), then rstd in fp64 by one thread
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, ss_hi, o);
+    const float ol = __shfl_xor_sync(0xffffffffu, ss_lo, o);
+    df_add_df(ss_hi, ss_lo, oh, ol);
+  }
+  if ((tid & 31) == 0) {
+    red[2 * (tid >> 5)] = ss_hi;
+    red[2 * (tid >> 5) + 1] = ss_lo;
+  }
   __syncthreads();
-  const float total = (red[0] + red[1]) + (red[2] + red[3]);
-  const float rs = 1.0f / sqrtf(total / float(C) + eps);
-  if (tid == 0) rstd[row] = rs;
+  if (tid == 0) {
+    float h = red[0], l = red[1];
+    for (int w = 1; w < 4; ++w) df_add_df(h, l, red[2 * w], red[2 * w + 1]);
+    const double ms = (double(h) + double(l)) / double(C);
+    const double rs64 = 1.0 / sqrt(ms + double(eps));
+    const float rs_hi = float(rs64);
+    s_rstd[0] = rs_hi;
+    s_rstd[1] = float(rs64 - double(rs_hi));
+    rstd[row] = rs_hi;
+  }
+  __syncthreads();
+  const float rs_hi = s_rstd[0], rs_lo = s_rstd[1];
 
   float amax = 0.0f;
 #pragma unroll
@@ -89,9 +114,15 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float lo = (bf16_lo(rw[j]) * rs) * bf16_lo(gw[j]);
-        const float hi = (bf16_hi(rw[j]) * rs) * bf16_hi(gw[j]);
-        o[j] = pack_bf16x2(lo, hi);
+        uint32_t b[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float rg = (k ? bf16_hi(rw[j]) : bf16_lo(rw[j])) * (k ? bf16_hi(gw[j]) : bf16_lo(gw[j]));
+          const float th = rg * rs_hi;
+          const float tl = fmaf(rg, rs_lo, fmaf(rg, rs_hi, -th));
+          b[k] = bf16_round_df(th, tl);
+        }
+        o[j] = b[0] | (b[1] << 16);
         amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(o[j])), fabsf(bf16_hi(o[j]))));
       }
       stg16(y + base + size_t(c) * 8, make_uint4(o[0], o[1], o[2], o[3]));
