@@ -94,7 +94,7 @@ def check_full(q, cfg, with_res=True):
     if with_res:
         np.testing.assert_array_equal(bf(g["res_out"]), ref["r"])
     np.testing.assert_array_equal(y, ref["y"])                                  # bit-exact
-    np.testing.assert_array_equal(host(g["rstd"]), ref["rstd"])
+    np.testing.assert_allclose(host(g["rstd"]), ref["rstd"], rtol=2.0 ** -23, atol=0)
     np.testing.assert_array_equal(st[0:2], ref["stats_y"])                     # abs-max, scale
     np.testing.assert_array_equal(yq, ref["yq"])                               # codes
     # A3+A4 stage-wise: the fused h equals SwiGLU of the GPU's own unfused gate|up GEMM
@@ -191,7 +191,7 @@ def test_forward_llama3_8b_sampled(q):
     np.testing.assert_array_equal(bf(g["res_out"])[rows], r)
     y = bf(g["y"])[rows]
     np.testing.assert_array_equal(y, y_ref)
-    np.testing.assert_array_equal(host(g["rstd"])[rows], rstd_ref)
+    np.testing.assert_allclose(host(g["rstd"])[rows], rstd_ref, rtol=2.0 ** -23, atol=0)
     yq = host(g["yq"])[rows]
     np.testing.assert_array_equal(yq, oracle.quantize_with_abs_max(y, st[0])[0])
     h = bf(g["h"])[rows]

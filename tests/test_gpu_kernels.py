@@ -50,7 +50,7 @@ def test_rmsnorm_absmax(q, N, C, with_res):
     yg = bf(y)
     # y is rounded once from an almost exact value: bit-identical to the oracle
     np.testing.assert_array_equal(yg, y_ref)
-    np.testing.assert_array_equal(host(rstd), rstd_ref)
+    np.testing.assert_allclose(host(rstd), rstd_ref, rtol=2.0 ** -23, atol=0)
     st = host(stats)
     assert st[0] == amax_ref
     assert st[1] == 123.0                                           # scale slot untouched

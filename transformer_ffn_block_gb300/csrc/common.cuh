@@ -74,10 +74,18 @@ QFFN_DEVI void df_add_df(float& hi, float& lo, float bhi, float blo) {
   hi = s + e;
   lo = e - (hi - s);
 }
-// Round th + tl (|tl| <= ulp(th) / 2) to bf16, nearest-even, as one rounding:
-// th's own rounding decides unless th sits exactly halfway between two bf16
-// values, where the sign of tl (relative to th) picks the side.
+// (hi, lo) <- fl(hi + lo) and its exact error; needs |hi| >= |lo| (Dekker).
+QFFN_DEVI void fast_two_sum(float& hi, float& lo) {
+  const float s = hi + lo;
+  lo = lo - (s - hi);
+  hi = s;
+}
+// Round the double-float th + tl to bf16, nearest-even, as one rounding.  After
+// renormalisation th is the float nearest to th + tl, so th's own bf16
+// rounding is the right one unless th sits exactly halfway between two bf16
+// values; there the sign of tl (relative to th) picks the side.
 QFFN_DEVI uint32_t bf16_round_df(float th, float tl) {
+  fast_two_sum(th, tl);
   const uint32_t bits = __float_as_uint(th);
   uint32_t b = f32_to_bf16(th);
   if ((bits & 0xFFFFu) == 0x8000u && tl != 0.0f) b = (bits >> 16) + (((tl > 0.0f) == (th > 0.0f)) ? 1u : 0u);

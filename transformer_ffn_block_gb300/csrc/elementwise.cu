@@ -36,10 +36,10 @@ __device__ __forceinline__ float block_reduce_max(float v, float* red) {
 //
 // y is rounded once from an almost exact value, so it agrees with the
 // correctly rounded r * rstd * g: each r^2 is exact in fp32 and is summed as
-// a double-float; mean, eps, sqrt and reciprocal are done once per row in
-// fp64 and rstd is split into a float pair (hi, lo); r * g is exact in fp32
-// and (r * g) * (hi + lo) is formed as a double-float with two fmas before
-// the single rounding to bf16.
+// a double-float (about 48 bits); mean, eps and 1/sqrt are formed once per
+// row as a double-float (rstd = hi + lo, about 43 bits); r * g is exact in
+// fp32 and (r * g) * (hi + lo) is formed as a double-float with two fmas
+// before the single rounding to bf16.
 template <int V>
 __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_t* y, float* rstd,
                                                       float* stats, const uint16_t* res_in,
@@ -93,11 +93,26 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_
   if (tid == 0) {
     float h = red[0], l = red[1];
     for (int w = 1; w < 4; ++w) df_add_df(h, l, red[2 * w], red[2 * w + 1]);
-    const double ms = (double(h) + double(l)) / double(C);
-    const double rs64 = 1.0 / sqrt(ms + double(eps));
-    const float rs_hi = float(rs64);
+    // ms = (h + l) / C as a double-float: q1 + q2
+    const float fc = float(C);
+    const float q1 = h / fc;
+    const float q2 = (fmaf(-q1, fc, h) + l) / fc;   // the fma residual h - q1*C is exact
+    // m = ms + eps
+    float mh, ml;
+    two_sum(q1, eps, mh, ml);
+    ml += q2;
+    fast_two_sum(mh, ml);
+    // rstd = 1/sqrt(m): approximate reciprocal square root, then one Newton
+    // step r0 + r0 * (1 - m r0^2) / 2 with the residual formed from exact
+    // products (fma), good to about 2^-43 relative
+    const float r0 = rsqrtf(mh);
+    const float p = r0 * r0, pl = fmaf(r0, r0, -p);          // r0^2 = p + pl exactly
+    const float t = mh * p, tl = fmaf(mh, p, -t);            // mh * p = t + tl exactly
+    const float e = ((1.0f - t) - tl) - fmaf(mh, pl, ml * p);
+    float rs_hi = r0, rs_lo = 0.5f * r0 * e;
+    fast_two_sum(rs_hi, rs_lo);
     s_rstd[0] = rs_hi;
-    s_rstd[1] = float(rs64 - double(rs_hi));
+    s_rstd[1] = rs_lo;
     rstd[row] = rs_hi;
   }
   __syncthreads();
