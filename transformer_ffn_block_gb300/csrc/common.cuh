@@ -85,11 +85,47 @@ QFFN_DEVI void fast_two_sum(float& hi, float& lo) {
 // rounding is the right one unless th sits exactly halfway between two bf16
 // values; there the sign of tl (relative to th) picks the side.
 QFFN_DEVI uint32_t bf16_round_df(float th, float tl) {
-  fast_two_sum(th, tl);
+  if (tl != 0.0f) fast_two_sum(th, tl);   // (tl == 0 keeps the sign of a zero th)
   const uint32_t bits = __float_as_uint(th);
   uint32_t b = f32_to_bf16(th);
   if ((bits & 0xFFFFu) == 0x8000u && tl != 0.0f) b = (bits >> 16) + (((tl > 0.0f) == (th > 0.0f)) ? 1u : 0u);
   return b;
+}
+
+// ----------------------------------------------------------------- packed fp32 pairs
+// Two floats in one 64-bit register, operated on by the f32x2 instructions.
+QFFN_DEVI uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+QFFN_DEVI void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+QFFN_DEVI uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+QFFN_DEVI uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+QFFN_DEVI uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// the two bf16 halves of a 32-bit word as a float pair (low half first)
+QFFN_DEVI uint64_t bf16x2_to_f2(uint32_t w) { return f2_pack(bf16_lo(w), bf16_hi(w)); }
+// (hi, lo) += x lane by lane, two_sum on pairs
+QFFN_DEVI void f2_df_add(uint64_t& hi, uint64_t& lo, uint64_t x) {
+  const uint64_t s = f2_add(hi, x);
+  const uint64_t bb = f2_sub(s, hi);
+  const uint64_t e = f2_add(f2_sub(hi, f2_sub(s, bb)), f2_sub(x, bb));
+  hi = s;
+  lo = f2_add(lo, e);
 }
 
 // ----------------------------------------------------------------- SwiGLU

@@ -52,7 +52,8 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_
   const int tid = threadIdx.x;
   const size_t base = size_t(row) * size_t(C);
   uint4 rv[V];
-  float ss_hi = 0.0f, ss_lo = 0.0f;
+  // two packed double-float accumulators: four independent (hi, lo) lanes
+  uint64_t acc_hi[2] = {0ull, 0ull}, acc_lo[2] = {0ull, 0ull};
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int c = tid + i * 128;
@@ -72,11 +73,21 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_
       const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const float lo = bf16_lo(w[j]), hi = bf16_hi(w[j]);
-        df_add(ss_hi, ss_lo, lo * lo);     // squares of bf16 values are exact in fp32
-        df_add(ss_hi, ss_lo, hi * hi);
+        const uint64_t v = bf16x2_to_f2(w[j]);
+        f2_df_add(acc_hi[j & 1], acc_lo[j & 1], f2_mul(v, v));   // squares of bf16 are exact
       }
     }
+  }
+  float ss_hi, ss_lo;
+  {
+    float h[4], l[4];
+    f2_unpack(acc_hi[0], h[0], h[1]);
+    f2_unpack(acc_hi[1], h[2], h[3]);
+    f2_unpack(acc_lo[0], l[0], l[1]);
+    f2_unpack(acc_lo[1], l[2], l[3]);
+    ss_hi = h[0];
+    ss_lo = l[0];
+    for (int k = 1; k < 4; ++k) df_add_df(ss_hi, ss_lo, h[k], l[k]);
   }
   // block sum of squares (double-float), then rstd in fp64 by one thread
 #pragma unroll
@@ -117,6 +128,7 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_
   }
   __syncthreads();
   const float rs_hi = s_rstd[0], rs_lo = s_rstd[1];
+  const uint64_t rs_hi2 = f2_pack(rs_hi, rs_hi);
 
   float amax = 0.0f;
 #pragma unroll
@@ -129,15 +141,22 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_
       uint32_t o[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint32_t b[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const float rg = (k ? bf16_hi(rw[j]) : bf16_lo(rw[j])) * (k ? bf16_hi(gw[j]) : bf16_lo(gw[j]));
-          const float th = rg * rs_hi;
-          const float tl = fmaf(rg, rs_lo, fmaf(rg, rs_hi, -th));
-          b[k] = bf16_round_df(th, tl);
+        // t = (r * g) * rstd: r * g is exact; th = fl((r * g) * rs_hi) is within two
+        // float ulps of t, so its bf16 rounding is t's unless th lies within three
+        // ulps of a bf16 halfway point (low 16 bits near 0x8000); those rare
+        // elements are finished with the exact double-float product
+        const uint64_t rg = f2_mul(bf16x2_to_f2(rw[j]), bf16x2_to_f2(gw[j]));
+        float th0, th1;
+        f2_unpack(f2_mul(rg, rs_hi2), th0, th1);
+        o[j] = pack_bf16x2(th0, th1);
+        const uint32_t b0 = __float_as_uint(th0), b1 = __float_as_uint(th1);
+        if (((b0 + 0x8003u) & 0xFFFFu) <= 6u || ((b1 + 0x8003u) & 0xFFFFu) <= 6u) {
+          float rg0, rg1;
+          f2_unpack(rg, rg0, rg1);
+          const uint32_t lo = bf16_round_df(th0, fmaf(rg0, rs_lo, fmaf(rg0, rs_hi, -th0)));
+          const uint32_t hi = bf16_round_df(th1, fmaf(rg1, rs_lo, fmaf(rg1, rs_hi, -th1)));
+          o[j] = lo | (hi << 16);
         }
-        o[j] = b[0] | (b[1] << 16);
         amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(o[j])), fabsf(bf16_hi(o[j]))));
       }
       stg16(y + base + size_t(c) * 8, make_uint4(o[0], o[1], o[2], o[3]));
