@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqffn.so")
 
 SOURCES = ["api.cu", "elementwise.cu", "gemm_fp8.cu", "decode.cu", "decode_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "launch.h")] + [os.path.join(INCLUDE, "qffn.h")]
+HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "launch.h", "pipeline.cuh")] + [os.path.join(INCLUDE, "qffn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3",
                  "-I" + INCLUDE, "--expt-relaxed-constexpr"]

@@ -72,9 +72,10 @@ int qffn_abi_version(void) { return kAbiVersion; }
 
 qffn_status qffn_check_status(qffn_stream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return QFFN_ERR_CUDA;
-  unsigned int st = 0;
+  unsigned int st = 0, sd = 0;
   if (qffn::gemm_take_status(&st) != cudaSuccess) return QFFN_ERR_CUDA;
-  return st != 0 ? QFFN_ERR_TIMEOUT : QFFN_OK;
+  if (qffn::decode_take_status(&sd) != cudaSuccess) return QFFN_ERR_CUDA;
+  return (st | sd) != 0 ? QFFN_ERR_TIMEOUT : QFFN_OK;
 }
 
 qffn_status qffn_rmsnorm_absmax(uint16_t* res_out, uint16_t* y, float* rstd, float* stats,
@@ -244,9 +245,10 @@ qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream
   return from_cuda(qffn::launch_silu_mul(g, u, n, false, stream));
 }
 
+// decode workspace: g [H] bf16 | u [H] bf16 | grid-barrier counter, each 256-byte aligned
 size_t qffn_decode_workspace_size(int64_t C, int64_t H) {
   if (C < 16 || H < 16 || C > 32768 || H > 32768) return 0;
-  return round_up(size_t(H) * 2, 256) + size_t(H) * 2;
+  return 2 * round_up(size_t(H) * 2, 256) + 256;
 }
 
 qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
@@ -261,13 +263,14 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
   QFFN_ALIGNED(out); QFFN_ALIGNED(x); QFFN_ALIGNED(w_gate); QFFN_ALIGNED(w_up); QFFN_ALIGNED(w_down);
   QFFN_ALIGNED4(s_gate); QFFN_ALIGNED4(s_up); QFFN_ALIGNED4(s_down);
   QFFN_ALIGNED(workspace);
-  uint16_t* g = static_cast<uint16_t*>(workspace);
-  uint16_t* u = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(workspace) + round_up(size_t(H) * 2, 256));
-  // A6 (stream-ordered after the caller's producer of x), then A7 and A8 as
-  // programmatic dependent launches so each launch overlaps its predecessor's tail.
-  QFFN_CUDA(qffn::launch_gemv(g, u, x, w_gate, s_gate, w_up, s_up, H, C, false, stream));
-  QFFN_CUDA(qffn::launch_silu_mul(g, u, H, true, stream));
-  return from_cuda(qffn::launch_gemv(out, nullptr, g, w_down, s_down, nullptr, nullptr, C, H, true, stream));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t vec = round_up(size_t(H) * 2, 256);
+  uint16_t* g = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* u = reinterpret_cast<uint16_t*>(ws + vec);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(ws + 2 * vec);
+  // A6, A7 and A8 in one cooperative launch (see decode.cu)
+  return from_cuda(qffn::launch_decode_fused(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C,
+                                             H, g, u, counter, stream));
 }
 
 }  // extern "C"

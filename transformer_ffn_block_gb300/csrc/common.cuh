@@ -139,6 +139,17 @@ QFFN_DEVI float silu_mul_f32(float g, float u) {
   return (g * sig) * u;
 }
 
+// h = bf16(silu(g) * u) for the 8 bf16 pairs of two 16-byte vectors.
+QFFN_DEVI uint4 swiglu8(uint4 g, uint4 u) {
+  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    o[j] = pack_bf16x2(silu_mul_f32(bf16_lo(gw[j]), bf16_lo(uw[j])),
+                       silu_mul_f32(bf16_hi(gw[j]), bf16_hi(uw[j])));
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // ----------------------------------------------------------------- abs-max
 // Non-negative floats order like their bit patterns as unsigned integers, so
 // a tensor abs-max is an atomicMax on the bits.

@@ -11,8 +11,9 @@
 //
 // The scratch array below lives in every GPU that loads the library, for as
 // long as the process runs.  All calls on a device share it and it keeps what
-// the last call wrote; the decode writes every scratch element it reads
-// before reading it, so nothing needs clearing between calls.  Calls whose
+// the last call wrote; the decode writes every g/u element before reading it,
+// and the barrier counter that must start at zero is cleared on the stream at
+// the start of every call.  Calls whose
 // execution overlaps on the GPU (different streams, no ordering between them)
 // use the same array and race; order them on one stream or with events.
 #include <mutex>
@@ -22,10 +23,11 @@
 
 namespace {
 
-// Largest intermediate size H this entry point accepts: g and u, H bf16 each.
+// Largest intermediate size H this entry point accepts: g and u, H bf16 each,
+// followed by one 32-bit counter (the decode kernel's grid barrier).
 constexpr int64_t kNoAllocMaxH = 32768;
 
-static __device__ __align__(256) uint16_t g_decode_scratch[2 * kNoAllocMaxH];
+static __device__ __align__(256) uint16_t g_decode_scratch[2 * kNoAllocMaxH + 128];
 
 // Device address of g_decode_scratch for each device, looked up once per
 // device with that device current.  In host code the array's name is only a
@@ -70,12 +72,10 @@ extern "C" qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t
   if (scratch_address(&scratch) != cudaSuccess) return QFFN_ERR_CUDA;
   uint16_t* g = scratch;
   uint16_t* u = scratch + kNoAllocMaxH;
-  // the same three launches as qffn_decode_forward, with the scratch array as workspace
-  if (qffn::launch_gemv(g, u, x, w_gate, s_gate, w_up, s_up, H, C, false, stream) != cudaSuccess)
-    return QFFN_ERR_CUDA;
-  if (qffn::launch_silu_mul(g, u, H, true, stream) != cudaSuccess) return QFFN_ERR_CUDA;
-  if (qffn::launch_gemv(out, nullptr, g, w_down, s_down, nullptr, nullptr, C, H, true, stream) !=
-      cudaSuccess)
+  unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + 2 * kNoAllocMaxH);
+  // the same launch as qffn_decode_forward, with the scratch array as workspace
+  if (qffn::launch_decode_fused(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, g, u,
+                                counter, stream) != cudaSuccess)
     return QFFN_ERR_CUDA;
   return QFFN_OK;
 }

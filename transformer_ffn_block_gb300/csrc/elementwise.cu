@@ -267,17 +267,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(uint8_t* q, flo
 }
 
 // ------------------------------------------------------------------ A4 (standalone)
-// 8 outputs per thread per step: 16 bytes of gate, 16 bytes of up.
-__device__ __forceinline__ uint4 swiglu8(uint4 g, uint4 u) {
-  const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
-  uint32_t o[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    o[j] = pack_bf16x2(silu_mul_f32(bf16_lo(gw[j]), bf16_lo(uw[j])),
-                       silu_mul_f32(bf16_hi(gw[j]), bf16_hi(uw[j])));
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
+// 8 outputs per thread per step: 16 bytes of gate, 16 bytes of up (swiglu8 in common.cuh).
 __device__ __forceinline__ float absmax8(uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   float m = 0.0f;

@@ -32,6 +32,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "pipeline.cuh"
 
 namespace qffn {
 namespace {
@@ -69,52 +70,10 @@ struct GemmArgs {
   int tiles_m, tiles_n, num_tiles, num_kb;
 };
 
-QFFN_DEVI uint32_t smem_u32(const void* p) { return uint32_t(__cvta_generic_to_shared(p)); }
-
-QFFN_DEVI void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-QFFN_DEVI void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-QFFN_DEVI void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-QFFN_DEVI bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-QFFN_DEVI unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Waits for the phase of `bar` with the given parity to complete.  Returns
-// false if the CTA abort flag is up (when honoured) or the time limit runs
-// out; running out raises the abort flag and the device status word.
+// Bounded wait on a pipeline barrier of this kernel (status word g_status).
 QFFN_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                          bool honour_abort = true, unsigned long long limit = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (honour_abort && *abort_flag) return false;
-      if (globaltimer() - t0 > limit) {
-        *abort_flag = 1;
-        atomicOr(&g_status, 1u);
-        return false;
-      }
-    }
-  }
+  return mbar_wait_bounded(bar, parity, abort_flag, &g_status, honour_abort, limit);
 }
 
 QFFN_DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
@@ -218,8 +177,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_init_fence();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
