@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #define QFFN_DEVI __device__ __forceinline__
+#define QFFN_DEVI_HOST __host__ __device__ __forceinline__
 
 namespace qffn {
 

@@ -30,15 +30,17 @@
 namespace qffn {
 namespace {
 
-constexpr int kConsumers = 256;
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kRingBytes = 192 * 1024;
-constexpr int kSlotTarget = 32 * 1024;
-constexpr int kMaxRowsPerStage = 8;
-constexpr int kMaxK = 8;                   // chunks per thread per row: cols <= 32768
-constexpr int kRedFloats = 2 * kMaxRowsPerStage * 2 * 8;
+constexpr int kSlotTarget = 16 * 1024;
+constexpr int kMaxRowsPerStage = 16;
+constexpr int kMaxSlots = 32;
+constexpr int kMaxK = 4;                   // chunks per lane per row (x kept in registers)
 constexpr unsigned long long kWaitNs = 2000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
+constexpr int kAllConsumersBarrier = 15;
 
 __device__ unsigned int g_decode_status;
 
@@ -94,14 +96,24 @@ QFFN_DEVI void row_range(int rows, int& r0, int& r1) {
   r1 = int((int64_t(rows) * (blockIdx.x + 1)) / gridDim.x);
 }
 
+// warps per row for a row of `cols` bytes: enough that a lane holds at most
+// kMaxK 16-byte chunks, rounded up to a power of two
+QFFN_DEVI_HOST int team_warps(int cols) {
+  const int nchunk = cols >> 4;
+  int s = 1;
+  while (s * 32 * kMaxK < nchunk) s <<= 1;
+  return s;
+}
+
 template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~uintptr_t(127));
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + size_t(p.nslots) * p.slot_bytes);
-  float* red = reinterpret_cast<float*>(bars + 2 * p.nslots);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kRedFloats);
+  unsigned int* slot_cnt = reinterpret_cast<unsigned int*>(bars + 2 * p.nslots);
+  float* red = reinterpret_cast<float*>(slot_cnt + kMaxSlots);   // [warp][2 bufs][2 mats]
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kConsumerWarps * 4);
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t ring0 = smem_u32(ring);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -109,15 +121,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
 
   if (tid == 0) {
     for (int s = 0; s < p.nslots; ++s) {
-      mbar_init(bar0 + 8u * s, 1);                 // full: producer's expect_tx
-      mbar_init(bar0 + 8u * (p.nslots + s), 1);    // empty: one consumer arrival
+      mbar_init(bar0 + 8u * s, 1);                 // full: the producer's expect_tx
+      mbar_init(bar0 + 8u * (p.nslots + s), 1);    // empty: the last row of the slot
+      slot_cnt[s] = 0;
     }
     *abort_flag = 0;
     mbar_init_fence();
   }
   __syncthreads();
 
-  if (warp == kConsumers / 32) {
+  if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t issued = 0, issued_par = 0;
@@ -156,14 +169,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
   }
 
   // -------------------------------------------------------------- consumers
-  int it = 0;
+  // Teams of S warps own whole rows: row i of this CTA's range goes to team
+  // i % NT.  A team finishes its row on its own (warp sums, then the team's
+  // leader adds its S warp sums in order) and the last row of a slot to finish
+  // hands the slot back to the producer.  Consumers never leave early: after a
+  // timed-out wait every later wait returns at once and the kernel runs out.
+  int stage_base = 0;
   for (int ph = 0; ph < nphases; ++ph) {
     const Phase& P = p.ph[ph];
+    const int S = team_warps(P.cols);
+    const int NT = kConsumerWarps / S;
+    const int team = warp / S, wt = warp % S;
+    const int tt = wt * 32 + lane;                  // thread index within the team
+    const int stride = S * 32;                      // chunk stride of a lane
     const int nchunk = P.cols >> 4;
     if (FUSED && ph == 1) {
       // grid-wide barrier: every CTA has written its g and u rows
-      named_sync(1, kConsumers);
-      if (tid == 0) {
+      named_sync(kAllConsumersBarrier, kConsumers);
+      if (tid == 0 && !*abort_flag) {
         __threadfence();
         atomicAdd(p.counter, 1u);
         const unsigned long long t0 = globaltimer();
@@ -177,14 +200,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
         }
         __threadfence();
       }
-      named_sync(1, kConsumers);
-      if (*abort_flag) return;
+      named_sync(kAllConsumersBarrier, kConsumers);
     }
-    // this thread's x chunks for the whole phase
+    // this lane's x chunks for the whole phase
     uint4 xr[kMaxK][2];
 #pragma unroll
     for (int k = 0; k < kMaxK; ++k) {
-      const int c = tid + kConsumers * k;
+      const int c = tt + stride * k;
       if (c < nchunk) {
         if (FUSED && ph == 1) {
           const uint16_t* gp = p.g + size_t(c) * 16;
@@ -201,40 +223,59 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
     }
     int r0, r1;
     row_range(P.rows, r0, r1);
-    for (int row = r0; row < r1; row += P.rps, ++it) {
-      const int n = min(P.rps, r1 - row);
-      const int s = it % p.nslots;
-      const uint32_t par = uint32_t(it / p.nslots) & 1u;
+    const int nrows = r1 - r0;
+    int nrow_team = 0;
+    for (int i = team; i < nrows; i += NT, ++nrow_team) {
+      const int st = stage_base + i / P.rps;
+      const int s = st % p.nslots;
+      const uint32_t par = uint32_t(st / p.nslots) & 1u;
+      const int ri = i % P.rps;
       mbar_wait_bounded(bar0 + 8u * s, par, abort_flag, &g_decode_status, true, kWaitNs);
       const uint32_t slot = ring0 + uint32_t(s) * uint32_t(p.slot_bytes);
-      float* rb = red + (it & 1) * (kRedFloats / 2);
-      for (int r = 0; r < n; ++r) {
+      float part[2];
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          if (m < P.nmat) {
-            const uint32_t wrow = slot + uint32_t(m * P.rps + r) * uint32_t(P.cols);
-            float acc = 0.0f;
+      for (int m = 0; m < 2; ++m) {
+        part[m] = 0.0f;
+        if (m < P.nmat) {
+          const uint32_t wrow = slot + uint32_t(m * P.rps + ri) * uint32_t(P.cols);
+          float a0 = 0.0f, a1 = 0.0f;
 #pragma unroll
-            for (int k = 0; k < kMaxK; ++k) {
-              const int c = tid + kConsumers * k;
-              if (c < nchunk) acc = dot16(ld_shared16(wrow + uint32_t(c) * 16u), xr[k][0], xr[k][1], acc);
-            }
-            acc = warp_sum(acc);
-            if (lane == 0) rb[(r * 2 + m) * 8 + warp] = acc;
+          for (int k = 0; k < kMaxK; k += 2) {
+            const int c0 = tt + stride * k, c1 = c0 + stride;
+            if (c0 < nchunk) a0 = dot16(ld_shared16(wrow + uint32_t(c0) * 16u), xr[k][0], xr[k][1], a0);
+            if (c1 < nchunk) a1 = dot16(ld_shared16(wrow + uint32_t(c1) * 16u), xr[k + 1][0], xr[k + 1][1], a1);
+          }
+          part[m] = warp_sum(a0 + a1);
+        }
+      }
+      float tot[2] = {part[0], part[1]};
+      if (S > 1) {
+        float* rb = red + 4 * team * S;                   // this team's [S warps][2 bufs][2]
+        if (lane == 0) {
+          rb[wt * 4 + (nrow_team & 1) * 2 + 0] = part[0];
+          rb[wt * 4 + (nrow_team & 1) * 2 + 1] = part[1];
+        }
+        named_sync(1 + team, S * 32);
+        if (tt == 0) {
+          tot[0] = tot[1] = 0.0f;
+          for (int w = 0; w < S; ++w) {
+            tot[0] += rb[w * 4 + (nrow_team & 1) * 2 + 0];
+            tot[1] += rb[w * 4 + (nrow_team & 1) * 2 + 1];
           }
         }
       }
-      named_sync(1, kConsumers);
-      if (*abort_flag) return;              // uniform: decided after the barrier
-      if (tid == 0) mbar_arrive(bar0 + 8u * (p.nslots + s));
-      if (tid < n * P.nmat) {
-        const int r = tid / P.nmat, m = tid - r * P.nmat;
-        float acc = 0.0f;
-#pragma unroll
-        for (int w = 0; w < 8; ++w) acc += rb[(r * 2 + m) * 8 + w];
-        P.out[m][row + r] = f32_to_bf16(P.s[m][row + r] * acc);
+      if (tt == 0) {
+        const int row = r0 + i;
+        for (int m = 0; m < P.nmat; ++m) P.out[m][row] = f32_to_bf16(P.s[m][row] * tot[m]);
+        // this row's slot data has been read by the whole team (it fed the sums)
+        const int n_in_slot = min(P.rps, nrows - (i / P.rps) * P.rps);
+        if (atomicAdd(&slot_cnt[s], 1u) == unsigned(n_in_slot - 1)) {
+          slot_cnt[s] = 0;
+          mbar_arrive(bar0 + 8u * (p.nslots + s));
+        }
       }
     }
+    stage_base += (nrows + P.rps - 1) / P.rps;
   }
 }
 
@@ -254,8 +295,9 @@ cudaError_t launch_stream(Params& p, int nphases, cudaStream_t s) {
     if (b > p.slot_bytes) p.slot_bytes = b;
   }
   p.nslots = kRingBytes / p.slot_bytes;
-  if (p.nslots > 16) p.nslots = 16;
-  const size_t smem = size_t(p.nslots) * p.slot_bytes + 128 + 16 * p.nslots + kRedFloats * 4 + 16;
+  if (p.nslots > kMaxSlots) p.nslots = kMaxSlots;
+  const size_t smem = size_t(p.nslots) * p.slot_bytes + 128 + 16 * p.nslots + 4 * kMaxSlots +
+                      4 * kConsumerWarps * 4 + 16;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
