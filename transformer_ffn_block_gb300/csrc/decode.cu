@@ -4,25 +4,34 @@
 //
 //   out[r] = bf16(row_scale[r] * sum_k W[r,k] * x[k]),  W E4M3, x bf16.
 //
-// One persistent CTA per SM streams a contiguous range of weight rows from
-// HBM into a shared-memory ring with bulk copies (one producer thread), while
-// eight consumer warps reduce the rows from shared memory: consumer thread t
-// owns the 16-byte chunks t, t+256, ... of every row and keeps the matching
-// x values in registers for the whole pass.  Per row the arithmetic is fixed
-// (chunks in order, one fma chain per thread, a warp butterfly, then the
-// eight warp sums in order), so the single, dual and fused forms below give
-// the same bits for the same row.
+// Streaming: one persistent CTA per SM.  A producer thread moves 8-row blocks
+// of the weight matrices (split along K into pieces of at most 2048 bytes)
+// from HBM into a shared-memory ring with bulk copies; 16 consumer warps
+// reduce each piece with warp-level tensor-core MMAs (m16n8k16, f16 inputs,
+// fp32 accumulation): the 8 weight rows are the 8 columns of the B operand
+// (E4M3 -> f16 is exact), x is row 0 of the A operand, so one MMA does 8 rows
+// x 16 columns and a warp needs 1 shared load, 2 converts and 1 MMA per 128
+// weight bytes.  x enters as f16 after an exact power-of-two scaling 2^k
+// chosen from max|x| (so every x with |x| >= max|x| 2^-29 is exact in f16 and
+// nothing overflows); 2^-k is applied to the finished sum.
 //
-// The fused decode form runs both halves of the FFN in one cooperative
-// launch: phase 0 is the dual gate/up GEMV (g, u to the workspace), then a
-// grid-wide barrier, then phase 1 is the down GEMV whose input h =
-// bf16(silu(g) * u) each thread forms for its own chunks.  The producer does
-// not wait at the barrier: it keeps streaming the down weights (which do not
-// depend on h) into the ring, so HBM stays busy across the phase boundary.
+// Per row the arithmetic depends only on the row length: the K split, the
+// columns each warp covers, the MMA order, the warp sums added in warp order
+// and the split partials added in split order.  So the single, dual and fused
+// forms give the same bits for the same row.
+//
+// The fused decode runs the whole FFN in one cooperative launch: phase 0 is
+// the dual gate/up GEMV (g, u to the workspace), then a grid-wide barrier,
+// then phase 1 is the down GEMV on h = bf16(silu(g) * u), which every CTA
+// forms for the whole vector.  The producer keeps streaming down weights into
+// the ring during the barrier.  Phase 1 hands out (8-row block, K piece) units
+// so the work splits evenly over the SMs; the CTA finishing the last piece of
+// a block adds the pieces' partial sums in piece order.
 //
 // Every wait is bounded (about 2 s); on expiry the kernel raises its device
-// status word, all consumers leave together after their next barrier, and the
-// producer drains its copies before returning.
+// status word and runs to the end without further waiting.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "launch.h"
 #include "pipeline.cuh"
@@ -33,14 +42,12 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
-constexpr int kRingBytes = 192 * 1024;
-constexpr int kSlotTarget = 16 * 1024;
-constexpr int kMaxRowsPerStage = 16;
-constexpr int kMaxSlots = 32;
-constexpr int kMaxK = 4;                   // chunks per lane per row (x kept in registers)
+constexpr int kBlockRows = 8;              // weight rows per MMA (the n8 of m16n8k16)
+constexpr int kPieceMax = 2048;            // bytes of K per piece
+constexpr int kSmemBudget = 226 * 1024;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
-constexpr int kAllConsumersBarrier = 15;
+constexpr int kAllConsumers = 15;          // named barrier of the 16 consumer warps
 
 __device__ unsigned int g_decode_status;
 
@@ -48,7 +55,10 @@ struct Phase {
   const uint8_t* w[2];
   const float* s[2];
   uint16_t* out[2];
-  int rows, cols, nmat, rps;
+  int rows, cols, nmat;
+  int pieces, piece;      // K pieces per row and their width (bytes, multiple of 256 but the last)
+  int nblocks;            // ceil(rows / 8)
+  int split;              // 1: units are (block, piece) spread over CTAs; 0: units are blocks
 };
 
 struct Params {
@@ -56,53 +66,107 @@ struct Params {
   const uint16_t* x;         // phase-0 input
   const uint16_t* g;         // fused: phase-1 input is silu(g) * u
   const uint16_t* u;
-  unsigned int* counter;     // fused: grid barrier counter (zeroed before launch)
-  int slot_bytes, nslots;
+  unsigned int* counter;     // fused: [0] grid barrier, [1 + b] pieces done of block b (zeroed)
+  float* partial;            // fused: [pieces][rows] split partial sums of phase 1
+  int slot_bytes, nslots, xcap;
 };
 
-QFFN_DEVI uint4 ld_shared16(uint32_t addr) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+QFFN_DEVI uint32_t ld_shared32(uint32_t addr) {
+  uint32_t r;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(addr));
   return r;
 }
-// L2-coherent load (data written by other CTAs of the same kernel)
+QFFN_DEVI uint2 ld_shared64(uint32_t addr) {
+  uint2 r;
+  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
+  return r;
+}
+// L2-coherent loads (data written by other CTAs of the same kernel)
 QFFN_DEVI uint4 ld_cg16(const void* p) {
   uint4 r;
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
   return r;
 }
+QFFN_DEVI float ld_cg_f32(const float* p) {
+  float r;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p) : "memory");
+  return r;
+}
+QFFN_DEVI uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(uint16_t(two_codes)));
+  return r;
+}
+// D += A(16x16, f16, row) * B(16x8, f16, col), fp32 accumulate
+QFFN_DEVI void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
+      " {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 
-// acc += sum of the 16 products of one weight chunk with its 16 x values
-// (x as 16 bf16 in two uint4), in element order.
-QFFN_DEVI float dot16(uint4 w, uint4 xa, uint4 xb, float acc) {
-  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-  const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float f0, f1, f2, f3;
-    e4m3x4_to_f32(ww[j], f0, f1, f2, f3);
-    acc = fmaf(f0, bf16_lo(xw[2 * j]), acc);
-    acc = fmaf(f1, bf16_hi(xw[2 * j]), acc);
-    acc = fmaf(f2, bf16_lo(xw[2 * j + 1]), acc);
-    acc = fmaf(f3, bf16_hi(xw[2 * j + 1]), acc);
+// contiguous share [u0, u1) of `n` units for this CTA
+QFFN_DEVI void unit_range(int n, int& u0, int& u1) {
+  u0 = int((int64_t(n) * blockIdx.x) / gridDim.x);
+  u1 = int((int64_t(n) * (blockIdx.x + 1)) / gridDim.x);
+}
+
+// The stages of a phase for this CTA, in order: (block, piece) pairs.
+struct StageIter {
+  int u, u1, pieces, split;
+  QFFN_DEVI StageIter(const Phase& P) : pieces(P.pieces), split(P.split) {
+    int a, b;
+    unit_range(P.split ? P.nblocks * P.pieces : P.nblocks, a, b);
+    u = P.split ? a : a * P.pieces;
+    u1 = P.split ? b : b * P.pieces;
   }
-  return acc;
-}
+  QFFN_DEVI bool more() const { return u < u1; }
+  QFFN_DEVI int block() const { return u / pieces; }
+  QFFN_DEVI int piece() const { return u % pieces; }
+  QFFN_DEVI void next() { ++u; }
+};
 
-QFFN_DEVI void row_range(int rows, int& r0, int& r1) {
-  r0 = int((int64_t(rows) * blockIdx.x) / gridDim.x);
-  r1 = int((int64_t(rows) * (blockIdx.x + 1)) / gridDim.x);
-}
 
-// warps per row for a row of `cols` bytes: enough that a lane holds at most
-// kMaxK 16-byte chunks, rounded up to a power of two
-QFFN_DEVI_HOST int team_warps(int cols) {
-  const int nchunk = cols >> 4;
-  int s = 1;
-  while (s * 32 * kMaxK < nchunk) s <<= 1;
-  return s;
+// x for a phase into shared memory as f16 scaled by 2^k (k from max|x|);
+// returns 2^-k.  Phase 1 of the fused decode forms x = bf16(silu(g) * u).
+template <bool FROM_GU>
+QFFN_DEVI float stage_x(uint16_t* xs, const uint16_t* x, const uint16_t* g, const uint16_t* u,
+                        int cols, float* xmax) {
+  const int tid = threadIdx.x;
+  float m = 0.0f;
+  for (int c = tid; c < (cols >> 3); c += kConsumers) {
+    uint4 v;
+    if (FROM_GU) v = swiglu8(ld_cg16(g + size_t(c) * 8), ld_cg16(u + size_t(c) * 8));
+    else v = ld16_once(x + size_t(c) * 8);
+    *reinterpret_cast<uint4*>(xs + size_t(c) * 8) = v;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+  m = warp_max(m);
+  if ((tid & 31) == 0) xmax[tid >> 5] = m;
+  named_sync(kAllConsumers, kConsumers);
+  float amax = 0.0f;
+  for (int w = 0; w < kConsumerWarps; ++w) amax = fmaxf(amax, xmax[w]);
+  int e = 0;
+  frexpf(amax, &e);                                   // amax = f * 2^e, f in [0.5, 1)
+  const int k = amax > 0.0f ? 15 - e : 0;             // amax * 2^k in [2^14, 2^15)
+  const float up = ldexpf(1.0f, k);
+  for (int c = tid; c < (cols >> 3); c += kConsumers) {
+    uint4 v = *reinterpret_cast<uint4*>(xs + size_t(c) * 8);
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __half2 h = __floats2half2_rn(bf16_lo(w[j]) * up, bf16_hi(w[j]) * up);
+      w[j] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(xs + size_t(c) * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  named_sync(kAllConsumers, kConsumers);
+  return ldexpf(1.0f, -k);
 }
 
 template <bool FUSED>
@@ -110,20 +174,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                              ~uintptr_t(127));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + size_t(p.nslots) * p.slot_bytes);
-  unsigned int* slot_cnt = reinterpret_cast<unsigned int*>(bars + 2 * p.nslots);
-  float* red = reinterpret_cast<float*>(slot_cnt + kMaxSlots);   // [warp][2 bufs][2 mats]
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kConsumerWarps * 4);
+  uint16_t* xs = reinterpret_cast<uint16_t*>(ring + size_t(p.nslots) * p.slot_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(xs + p.xcap);
+  float* red = reinterpret_cast<float*>(bars + 2 * p.nslots);     // [2 bufs][2 mats][16 warps][8 rows]
+  float* xmax = red + 2 * 2 * kConsumerWarps * kBlockRows;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(xmax + kConsumerWarps);
   const uint32_t bar0 = smem_u32(bars);
   const uint32_t ring0 = smem_u32(ring);
+  const uint32_t xs0 = smem_u32(xs);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int nphases = FUSED ? 2 : 1;
 
   if (tid == 0) {
     for (int s = 0; s < p.nslots; ++s) {
-      mbar_init(bar0 + 8u * s, 1);                 // full: the producer's expect_tx
-      mbar_init(bar0 + 8u * (p.nslots + s), 1);    // empty: the last row of the slot
-      slot_cnt[s] = 0;
+      mbar_init(bar0 + 8u * s, 1);                              // full: the producer's expect_tx
+      mbar_init(bar0 + 8u * (p.nslots + s), kConsumerWarps);    // empty: every consumer warp
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -138,24 +203,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
       bool ok = true;
       for (int ph = 0; ok && ph < nphases; ++ph) {
         const Phase& P = p.ph[ph];
-        int r0, r1;
-        row_range(P.rows, r0, r1);
-        for (int row = r0; row < r1; row += P.rps, ++it) {
-          const int n = min(P.rps, r1 - row);
+        for (StageIter si(P); si.more(); si.next(), ++it) {
+          const int b = si.block(), j = si.piece();
+          const int nr = min(kBlockRows, P.rows - b * kBlockRows);
+          const int width = min(P.piece, P.cols - j * P.piece);
           const int s = it % p.nslots;
           const uint32_t par = uint32_t(it / p.nslots) & 1u;
-          if (!mbar_wait_bounded(bar0 + 8u * (p.nslots + s), par ^ 1u, abort_flag, &g_decode_status,
-                                 true, kWaitNs)) {
+          if (!mbar_wait_bounded(bar0 + 8u * (p.nslots + s), par ^ 1u, abort_flag,
+                                 &g_decode_status, true, kWaitNs)) {
             ok = false;
             break;
           }
-          const uint32_t bytes = uint32_t(n) * uint32_t(P.cols);
           const uint32_t full = bar0 + 8u * s;
-          mbar_expect_tx(full, bytes * uint32_t(P.nmat));
+          mbar_expect_tx(full, uint32_t(nr * width * P.nmat));
           const uint32_t dst = ring0 + uint32_t(s) * uint32_t(p.slot_bytes);
           for (int m = 0; m < P.nmat; ++m)
-            bulk_load(dst + uint32_t(m) * uint32_t(P.rps) * uint32_t(P.cols),
-                      P.w[m] + size_t(row) * size_t(P.cols), bytes, full);
+            for (int r = 0; r < nr; ++r)
+              bulk_load(dst + uint32_t((m * kBlockRows + r) * P.piece),
+                        P.w[m] + size_t(b * kBlockRows + r) * size_t(P.cols) + size_t(j) * P.piece,
+                        uint32_t(width), full);
           issued |= 1u << s;
           issued_par = (issued_par & ~(1u << s)) | (par << s);
         }
@@ -169,23 +235,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
   }
 
   // -------------------------------------------------------------- consumers
-  // Teams of S warps own whole rows: row i of this CTA's range goes to team
-  // i % NT.  A team finishes its row on its own (warp sums, then the team's
-  // leader adds its S warp sums in order) and the last row of a slot to finish
-  // hands the slot back to the producer.  Consumers never leave early: after a
-  // timed-out wait every later wait returns at once and the kernel runs out.
-  int stage_base = 0;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  int it = 0;
+  float acc[2] = {0.0f, 0.0f};           // finishing threads: running sum over pieces
   for (int ph = 0; ph < nphases; ++ph) {
     const Phase& P = p.ph[ph];
-    const int S = team_warps(P.cols);
-    const int NT = kConsumerWarps / S;
-    const int team = warp / S, wt = warp % S;
-    const int tt = wt * 32 + lane;                  // thread index within the team
-    const int stride = S * 32;                      // chunk stride of a lane
-    const int nchunk = P.cols >> 4;
+    float down = 1.0f;
     if (FUSED && ph == 1) {
       // grid-wide barrier: every CTA has written its g and u rows
-      named_sync(kAllConsumersBarrier, kConsumers);
+      named_sync(kAllConsumers, kConsumers);
       if (tid == 0 && !*abort_flag) {
         __threadfence();
         atomicAdd(p.counter, 1u);
@@ -200,113 +258,118 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const Params p
         }
         __threadfence();
       }
-      named_sync(kAllConsumersBarrier, kConsumers);
+      named_sync(kAllConsumers, kConsumers);
+      down = stage_x<true>(xs, nullptr, p.g, p.u, P.cols, xmax);
+    } else {
+      down = stage_x<false>(xs, p.x, nullptr, nullptr, P.cols, xmax);
     }
-    // this lane's x chunks for the whole phase
-    uint4 xr[kMaxK][2];
-#pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-      const int c = tt + stride * k;
-      if (c < nchunk) {
-        if (FUSED && ph == 1) {
-          const uint16_t* gp = p.g + size_t(c) * 16;
-          const uint16_t* up = p.u + size_t(c) * 16;
-          xr[k][0] = swiglu8(ld_cg16(gp), ld_cg16(up));
-          xr[k][1] = swiglu8(ld_cg16(gp + 8), ld_cg16(up + 8));
-        } else {
-          xr[k][0] = ld16_once(p.x + size_t(c) * 16);
-          xr[k][1] = ld16_once(p.x + size_t(c) * 16 + 8);
-        }
-      } else {
-        xr[k][0] = xr[k][1] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    int r0, r1;
-    row_range(P.rows, r0, r1);
-    const int nrows = r1 - r0;
-    int nrow_team = 0;
-    for (int i = team; i < nrows; i += NT, ++nrow_team) {
-      const int st = stage_base + i / P.rps;
-      const int s = st % p.nslots;
-      const uint32_t par = uint32_t(st / p.nslots) & 1u;
-      const int ri = i % P.rps;
+    // columns of each piece a warp covers (a multiple of 16: whole MMA steps)
+    const int cw = ((P.piece / 16 + kConsumerWarps - 1) / kConsumerWarps) * 16;
+    for (StageIter si(P); si.more(); si.next(), ++it) {
+      const int b = si.block(), j = si.piece();
+      const int width = min(P.piece, P.cols - j * P.piece);
+      const int s = it % p.nslots;
+      const uint32_t par = uint32_t(it / p.nslots) & 1u;
       mbar_wait_bounded(bar0 + 8u * s, par, abort_flag, &g_decode_status, true, kWaitNs);
       const uint32_t slot = ring0 + uint32_t(s) * uint32_t(p.slot_bytes);
-      float part[2];
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        part[m] = 0.0f;
-        if (m < P.nmat) {
-          const uint32_t wrow = slot + uint32_t(m * P.rps + ri) * uint32_t(P.cols);
-          float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll
-          for (int k = 0; k < kMaxK; k += 2) {
-            const int c0 = tt + stride * k, c1 = c0 + stride;
-            if (c0 < nchunk) a0 = dot16(ld_shared16(wrow + uint32_t(c0) * 16u), xr[k][0], xr[k][1], a0);
-            if (c1 < nchunk) a1 = dot16(ld_shared16(wrow + uint32_t(c1) * 16u), xr[k + 1][0], xr[k + 1][1], a1);
-          }
-          part[m] = warp_sum(a0 + a1);
+      float d[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+      for (int c = warp * cw; c < min(warp * cw + cw, width); c += 16) {
+        uint32_t a0 = 0u, a2 = 0u;
+        if (lane < 4) {
+          const uint2 xv = ld_shared64(xs0 + 2u * uint32_t(j * P.piece + c + 4 * t4));
+          a0 = xv.x;
+          a2 = xv.y;
         }
-      }
-      float tot[2] = {part[0], part[1]};
-      if (S > 1) {
-        float* rb = red + 4 * team * S;                   // this team's [S warps][2 bufs][2]
-        if (lane == 0) {
-          rb[wt * 4 + (nrow_team & 1) * 2 + 0] = part[0];
-          rb[wt * 4 + (nrow_team & 1) * 2 + 1] = part[1];
-        }
-        named_sync(1 + team, S * 32);
-        if (tt == 0) {
-          tot[0] = tot[1] = 0.0f;
-          for (int w = 0; w < S; ++w) {
-            tot[0] += rb[w * 4 + (nrow_team & 1) * 2 + 0];
-            tot[1] += rb[w * 4 + (nrow_team & 1) * 2 + 1];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          if (m < P.nmat) {
+            const uint32_t wv = ld_shared32(slot + uint32_t((m * kBlockRows + g8) * P.piece + c + 4 * t4));
+            mma_16816(d[m], a0, 0u, a2, 0u, e4m3x2_to_f16x2(wv & 0xFFFFu), e4m3x2_to_f16x2(wv >> 16));
           }
         }
       }
-      if (tt == 0) {
-        const int row = r0 + i;
-        for (int m = 0; m < P.nmat; ++m) P.out[m][row] = f32_to_bf16(P.s[m][row] * tot[m]);
-        // this row's slot data has been read by the whole team (it fed the sums)
-        const int n_in_slot = min(P.rps, nrows - (i / P.rps) * P.rps);
-        if (atomicAdd(&slot_cnt[s], 1u) == unsigned(n_in_slot - 1)) {
-          slot_cnt[s] = 0;
-          mbar_arrive(bar0 + 8u * (p.nslots + s));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar0 + 8u * (p.nslots + s));   // this warp is done with the slot
+      float* rb = red + (it & 1) * (2 * kConsumerWarps * kBlockRows);
+      if (lane < 4) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          rb[(m * kConsumerWarps + warp) * kBlockRows + 2 * t4] = d[m][0];
+          rb[(m * kConsumerWarps + warp) * kBlockRows + 2 * t4 + 1] = d[m][1];
+        }
+      }
+      named_sync(kAllConsumers, kConsumers);
+      if (tid < kBlockRows * P.nmat) {
+        const int m = tid / kBlockRows, r = tid % kBlockRows;
+        const int row = b * kBlockRows + r;
+        float pj = 0.0f;
+        for (int w = 0; w < kConsumerWarps; ++w) pj += rb[(m * kConsumerWarps + w) * kBlockRows + r];
+        if (FUSED && P.split) {
+          if (row < P.rows) p.partial[size_t(j) * P.rows + row] = pj;
+        } else {
+          acc[m] = (j == 0) ? pj : acc[m] + pj;
+          if (j == P.pieces - 1 && row < P.rows)
+            P.out[m][row] = f32_to_bf16(P.s[m][row] * (acc[m] * down));
+        }
+      }
+      if (FUSED && P.split && warp == 0) {
+        // the CTA that adds the last piece of block b finishes it, adding the
+        // pieces' partial sums in piece order
+        __threadfence();
+        __syncwarp();
+        unsigned int done = 0;
+        if (lane == 0) done = atomicAdd(p.counter + 1 + b, 1u);
+        done = __shfl_sync(0xffffffffu, done, 0);
+        if (done == unsigned(P.pieces - 1)) {
+          __threadfence();
+          const int row = b * kBlockRows + lane;
+          if (lane < kBlockRows && row < P.rows) {
+            float t = 0.0f;
+            for (int jj = 0; jj < P.pieces; ++jj) {
+              const float v = ld_cg_f32(p.partial + size_t(jj) * P.rows + row);
+              t = (jj == 0) ? v : t + v;
+            }
+            P.out[0][row] = f32_to_bf16(P.s[0][row] * (t * down));
+          }
         }
       }
     }
-    stage_base += (nrows + P.rps - 1) / P.rps;
   }
 }
 
-int phase_rps(int cols, int nmat) {
-  int rps = kSlotTarget / (cols * nmat);
-  if (rps < 1) rps = 1;
-  if (rps > kMaxRowsPerStage) rps = kMaxRowsPerStage;
-  return rps;
+void set_phase(Phase& P, int rows, int cols, int nmat, int split) {
+  P.rows = rows;
+  P.cols = cols;
+  P.nmat = nmat;
+  P.pieces = (cols + kPieceMax - 1) / kPieceMax;
+  P.piece = ((cols + P.pieces - 1) / P.pieces + 255) / 256 * 256;
+  P.nblocks = (rows + kBlockRows - 1) / kBlockRows;
+  P.split = split;
 }
 
 template <bool FUSED>
 cudaError_t launch_stream(Params& p, int nphases, cudaStream_t s) {
   p.slot_bytes = 0;
+  p.xcap = 0;
   for (int i = 0; i < nphases; ++i) {
-    p.ph[i].rps = phase_rps(p.ph[i].cols, p.ph[i].nmat);
-    const int b = p.ph[i].rps * p.ph[i].cols * p.ph[i].nmat;
+    const int b = kBlockRows * p.ph[i].piece * p.ph[i].nmat;
     if (b > p.slot_bytes) p.slot_bytes = b;
+    if (p.ph[i].cols > p.xcap) p.xcap = p.ph[i].cols;
   }
-  p.nslots = kRingBytes / p.slot_bytes;
-  if (p.nslots > kMaxSlots) p.nslots = kMaxSlots;
-  const size_t smem = size_t(p.nslots) * p.slot_bytes + 128 + 16 * p.nslots + 4 * kMaxSlots +
-                      4 * kConsumerWarps * 4 + 16;
+  const int fixed = 128 + p.xcap * 2 + 2 * 2 * kConsumerWarps * kBlockRows * 4 + kConsumerWarps * 4 + 16;
+  p.nslots = (kSmemBudget - fixed - 16 * 32) / p.slot_bytes;
+  if (p.nslots > 32) p.nslots = 32;
+  if (p.nslots < 2) return cudaErrorInvalidValue;
+  const size_t smem = size_t(p.nslots) * p.slot_bytes + fixed + 16 * p.nslots;
   static int attr_done[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !(attr_done[dev] & 1)) {
+  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
     e = cudaFuncSetAttribute(gemv_stream_kernel<FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kRingBytes + 4096));
+                             kSmemBudget);
     if (e != cudaSuccess) return e;
-    attr_done[dev] |= 1;
+    attr_done[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(num_sms());
@@ -323,20 +386,27 @@ cudaError_t launch_stream(Params& p, int nphases, cudaStream_t s) {
 
 }  // namespace
 
+size_t decode_counter_bytes(int64_t C) {
+  return (size_t(1) + size_t((C + kBlockRows - 1) / kBlockRows)) * sizeof(unsigned int);
+}
+
+size_t decode_partial_bytes(int64_t C, int64_t H) {
+  return size_t((H + kPieceMax - 1) / kPieceMax) * size_t(C) * sizeof(float);
+}
+
 cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const uint8_t* w0,
                         const float* s0, const uint8_t* w1, const float* s1, int64_t rows,
                         int64_t cols, bool /*pdl*/, cudaStream_t s) {
   if (rows == 0) return cudaSuccess;
   Params p{};
-  p.ph[0].w[0] = w0;
-  p.ph[0].s[0] = s0;
-  p.ph[0].out[0] = out0;
-  p.ph[0].w[1] = w1;
-  p.ph[0].s[1] = s1;
-  p.ph[0].out[1] = out1;
-  p.ph[0].rows = int(rows);
-  p.ph[0].cols = int(cols);
-  p.ph[0].nmat = w1 != nullptr ? 2 : 1;
+  Phase& P = p.ph[0];
+  P.w[0] = w0;
+  P.s[0] = s0;
+  P.out[0] = out0;
+  P.w[1] = w1;
+  P.s[1] = s1;
+  P.out[1] = out1;
+  set_phase(P, int(rows), int(cols), w1 != nullptr ? 2 : 1, 0);
   p.x = x;
   return launch_stream<false>(p, 1, s);
 }
@@ -344,29 +414,29 @@ cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const
 cudaError_t launch_decode_fused(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
                                 const float* s_gate, const uint8_t* w_up, const float* s_up,
                                 const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
-                                uint16_t* g, uint16_t* u, unsigned int* counter, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(counter, 0, sizeof(unsigned int), s);
+                                uint16_t* g, uint16_t* u, unsigned int* counter, float* partial,
+                                cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(counter, 0, decode_counter_bytes(C), s);
   if (e != cudaSuccess) return e;
   Params p{};
-  p.ph[0].w[0] = w_gate;
-  p.ph[0].s[0] = s_gate;
-  p.ph[0].out[0] = g;
-  p.ph[0].w[1] = w_up;
-  p.ph[0].s[1] = s_up;
-  p.ph[0].out[1] = u;
-  p.ph[0].rows = int(H);
-  p.ph[0].cols = int(C);
-  p.ph[0].nmat = 2;
-  p.ph[1].w[0] = w_down;
-  p.ph[1].s[0] = s_down;
-  p.ph[1].out[0] = out;
-  p.ph[1].rows = int(C);
-  p.ph[1].cols = int(H);
-  p.ph[1].nmat = 1;
+  Phase& A = p.ph[0];
+  A.w[0] = w_gate;
+  A.s[0] = s_gate;
+  A.out[0] = g;
+  A.w[1] = w_up;
+  A.s[1] = s_up;
+  A.out[1] = u;
+  set_phase(A, int(H), int(C), 2, 0);
+  Phase& D = p.ph[1];
+  D.w[0] = w_down;
+  D.s[0] = s_down;
+  D.out[0] = out;
+  set_phase(D, int(C), int(H), 1, 1);
   p.x = x;
   p.g = g;
   p.u = u;
   p.counter = counter;
+  p.partial = partial;
   return launch_stream<true>(p, 2, s);
 }
 

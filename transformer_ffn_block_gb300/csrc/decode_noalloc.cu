@@ -11,9 +11,9 @@
 //
 // The scratch array below lives in every GPU that loads the library, for as
 // long as the process runs.  All calls on a device share it and it keeps what
-// the last call wrote; the decode writes every g/u element before reading it,
-// and the barrier counter that must start at zero is cleared on the stream at
-// the start of every call.  Calls whose
+// the last call wrote; the decode writes every g/u element and partial sum
+// before reading it, and the counters that must start at zero are cleared on
+// the stream at the start of every call.  Calls whose
 // execution overlaps on the GPU (different streams, no ordering between them)
 // use the same array and race; order them on one stream or with events.
 #include <mutex>
@@ -23,11 +23,19 @@
 
 namespace {
 
-// Largest intermediate size H this entry point accepts: g and u, H bf16 each,
-// followed by one 32-bit counter (the decode kernel's grid barrier).
+// Largest sizes this entry point accepts, and its scratch: g and u (H bf16
+// each), the decode kernel's counters (grid barrier and one per 8-row block of
+// the output) and its fp32 partial sums of the down projection (one per
+// 2048-column piece of h per output row).
 constexpr int64_t kNoAllocMaxH = 32768;
+constexpr int64_t kNoAllocMaxC = 8192;
+constexpr size_t kScratchG = 0;
+constexpr size_t kScratchU = size_t(kNoAllocMaxH) * 2;
+constexpr size_t kScratchCounter = 2 * kScratchU;
+constexpr size_t kScratchPartial = kScratchCounter + 4 * (1 + kNoAllocMaxC / 8) + 252;
+constexpr size_t kScratchBytes = kScratchPartial + 4 * (kNoAllocMaxH / 2048) * kNoAllocMaxC;
 
-static __device__ __align__(256) uint16_t g_decode_scratch[2 * kNoAllocMaxH + 128];
+static __device__ __align__(256) uint8_t g_decode_scratch[kScratchBytes];
 
 // Device address of g_decode_scratch for each device, looked up once per
 // device with that device current.  In host code the array's name is only a
@@ -35,7 +43,7 @@ static __device__ __align__(256) uint16_t g_decode_scratch[2 * kNoAllocMaxH + 12
 std::mutex g_scratch_mu;
 void* g_scratch_addr[64] = {nullptr};
 
-cudaError_t scratch_address(uint16_t** out) {
+cudaError_t scratch_address(uint8_t** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -47,7 +55,7 @@ cudaError_t scratch_address(uint16_t** out) {
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = p;
   }
-  *out = static_cast<uint16_t*>(g_scratch_addr[dev]);
+  *out = static_cast<uint8_t*>(g_scratch_addr[dev]);
   return cudaSuccess;
 }
 
@@ -63,19 +71,20 @@ extern "C" qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t
                                                    int64_t C, int64_t H, qffn_stream_t stream) {
   if (!out || !x || !w_gate || !s_gate || !w_up || !s_up || !w_down || !s_down)
     return QFFN_ERR_INVALID_ARG;
-  if (C % 16 != 0 || H % 16 != 0 || C < 16 || H < 16 || C > 32768 || H > kNoAllocMaxH)
+  if (C % 16 != 0 || H % 16 != 0 || C < 16 || H < 16 || C > kNoAllocMaxC || H > kNoAllocMaxH)
     return QFFN_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(out) || !aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) ||
       !aligned16(w_down) || !aligned4(s_gate) || !aligned4(s_up) || !aligned4(s_down))
     return QFFN_ERR_MISALIGNED;
-  uint16_t* scratch = nullptr;
+  uint8_t* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return QFFN_ERR_CUDA;
-  uint16_t* g = scratch;
-  uint16_t* u = scratch + kNoAllocMaxH;
-  unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + 2 * kNoAllocMaxH);
+  uint16_t* g = reinterpret_cast<uint16_t*>(scratch + kScratchG);
+  uint16_t* u = reinterpret_cast<uint16_t*>(scratch + kScratchU);
+  unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + kScratchCounter);
+  float* partial = reinterpret_cast<float*>(scratch + kScratchPartial);
   // the same launch as qffn_decode_forward, with the scratch array as workspace
   if (qffn::launch_decode_fused(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, g, u,
-                                counter, stream) != cudaSuccess)
+                                counter, partial, stream) != cudaSuccess)
     return QFFN_ERR_CUDA;
   return QFFN_OK;
 }
