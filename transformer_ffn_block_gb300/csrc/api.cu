@@ -48,7 +48,7 @@ void forward_offsets(int64_t N, int64_t C, int64_t H, size_t off[5]) {
 void decode_offsets(int64_t C, int64_t H, size_t off[4]) {
   off[0] = round_up(size_t(H) * 2, 256);                         // u
   off[1] = 2 * off[0];                                          // counters
-  off[2] = off[1] + round_up(qffn::decode_counter_bytes(C), 256);  // partials
+  off[2] = off[1] + round_up(qffn::decode_counter_bytes(C, H), 256);  // partials
   off[3] = off[2] + round_up(qffn::decode_partial_bytes(C, H), 256);
 }
 
