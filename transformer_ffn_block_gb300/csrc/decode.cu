@@ -42,7 +42,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kBlockRows = 8;              // weight rows per MMA (the n8 of m16n8k16)
 constexpr int kPiece = 512;                // columns of K per work unit
 constexpr int kStep = 64;                  // columns per load step (16 bytes per lane, 4 MMAs)
-constexpr int kBatch = 4;                  // load steps in flight per warp
+constexpr int kBatch = 8;                  // load steps in flight per warp (a whole piece)
 constexpr int kMaxCols = 32768;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
@@ -84,6 +84,11 @@ QFFN_DEVI float ld_cg_f32(const float* p) {
   float r;
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p) : "memory");
   return r;
+}
+QFFN_DEVI unsigned int atomic_add_acq_rel(unsigned int* p, unsigned int v) {
+  unsigned int old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 QFFN_DEVI uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   uint32_t r;
@@ -243,13 +248,13 @@ QFFN_DEVI void fused_phase(const Phase& P, uint32_t xs0, float down) {
           if (row < P.rows) P.partial[(size_t(m) * P.pieces + j) * P.rows + row] = d[m][e];
         }
     }
-    __threadfence();
+    // publish this piece (release) and learn whether it was the block's last
+    // (acquire): the warp barrier orders the other lanes' writes before lane 0
     __syncwarp();
     unsigned int done = 0;
-    if (lane == 0) done = atomicAdd(P.done + b, 1u);
+    if (lane == 0) done = atomic_add_acq_rel(P.done + b, 1u);
     done = __shfl_sync(0xffffffffu, done, 0);
     if (done == unsigned(P.pieces - 1)) {
-      __threadfence();
       if (lane < kBlockRows * NMAT) {
         const int m = lane / kBlockRows, row = b * kBlockRows + lane % kBlockRows;
         if (row < P.rows) {
