@@ -208,7 +208,7 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
  * Computes exactly what qffn_decode_forward computes (same kernel, same
  * bits), with its scratch (the g and u vectors, counters and fp32 partial
  * sums of the down projection) in a fixed array inside the library:
- * 6.2 MiB per GPU that loads the library, held until the process exits.
+ * 388 KiB per GPU that loads the library, held until the process exits.
  * H > 32768 or C > 8192 is rejected with QFFN_ERR_UNSUPPORTED_SHAPE; the other
  * size and alignment rules are those of qffn_decode_forward.  Nothing is
  * allocated by this call.

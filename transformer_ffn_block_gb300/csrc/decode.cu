@@ -40,9 +40,9 @@ namespace {
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kBlockRows = 8;              // weight rows per MMA (the n8 of m16n8k16)
-constexpr int kPiece = 512;                // columns of K per work unit
+constexpr int kPieceMax = 4096;            // columns of K per work unit at most
 constexpr int kStep = 64;                  // columns per load step (16 bytes per lane, 4 MMAs)
-constexpr int kBatch = 8;                  // load steps in flight per warp (a whole piece)
+constexpr int kSteps = 4;                  // load steps per warp per unit (cw <= 256)
 constexpr int kMaxCols = 32768;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
@@ -53,7 +53,8 @@ struct Phase {
   const float* s[2];
   uint16_t* out[2];
   int rows, cols, nmat;
-  int pieces;             // ceil(cols / 512)
+  int pieces, piece;      // K pieces per row and their width (ceil(cols / pieces) rounded to 64)
+  int cw;                 // columns of a piece per warp: piece / 16 rounded up to 64
   int nblocks;            // ceil(rows / 8)
   unsigned int* done;     // fused: pieces finished per block (zeroed before launch)
   float* partial;         // fused: [nmat][pieces][rows] piece partial sums
@@ -145,139 +146,163 @@ QFFN_DEVI float stage_x(uint16_t* xs, const uint16_t* x, const uint16_t* g, cons
   return ldexpf(1.0f, -k);
 }
 
-// One work unit for a warp: rows [8b, 8b+8) times columns [512j, 512j+512)
-// of each matrix.  On return lanes 0..3 hold in d[m][0], d[m][1] the partial
-// sums of rows 8b + 2*lane and 8b + 2*lane + 1 (scaled by 2^k).
+// Work unit of a CTA: rows [8b, 8b+8) times piece j of the columns.  Warp w
+// covers columns [w*cw, w*cw + cw) of the piece (cw = the piece width / 16
+// rounded up to 64), in 64-column steps; lane (g, t) loads 16 bytes of row
+// 8b + g at column 16t of each step, which feed four MMAs in order.
+struct Unit {
+  int b, j;
+};
+
+QFFN_DEVI Unit unit_of(const Phase& P, int u) { return Unit{u / P.pieces, u % P.pieces}; }
+
 template <int NMAT>
-QFFN_DEVI void piece_partial(const Phase& P, int b, int j, uint32_t xs0, int lane,
-                             float (&d)[2][4]) {
+QFFN_DEVI void load_unit(const Phase& P, Unit un, int warp, int lane, uint4 (&wv)[kSteps][NMAT]) {
   const int g = lane >> 2, t = lane & 3;
-  const int row = b * kBlockRows + g;
-  const bool row_ok = row < P.rows;
-  const int cbase = j * kPiece;
-  const int width = min(kPiece, P.cols - cbase);
-  const uint8_t* wr[2];
+  const int row = un.b * kBlockRows + g;
+  const int cbase = un.j * P.piece + warp * P.cw;
+  const int cend = min(P.cols, (un.j + 1) * P.piece);
 #pragma unroll
-  for (int m = 0; m < NMAT; ++m) wr[m] = P.w[m] + size_t(row_ok ? row : 0) * P.cols + cbase;
+  for (int q = 0; q < kSteps; ++q) {
+    const int col = cbase + q * kStep + 16 * t;
+    const bool ok = row < P.rows && q * kStep < P.cw && col < cend;
+#pragma unroll
+    for (int m = 0; m < NMAT; ++m)
+      wv[q][m] = ok ? ld16_ro_stream(P.w[m] + size_t(row) * P.cols + col) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// MMAs of one unit; lanes 0..3 end with the warp's partial sums of rows
+// 8b + 2*lane (d[m][0]) and 8b + 2*lane + 1 (d[m][1]).
+template <int NMAT>
+QFFN_DEVI void mma_unit(const Phase& P, Unit un, int warp, int lane, uint32_t xs0,
+                        const uint4 (&wv)[kSteps][NMAT], float (&d)[2][4]) {
+  const int t = lane & 3;
+  const int cbase = un.j * P.piece + warp * P.cw;
+  const int cend = min(P.cols, (un.j + 1) * P.piece);
 #pragma unroll
   for (int m = 0; m < 2; ++m) d[m][0] = d[m][1] = d[m][2] = d[m][3] = 0.0f;
-  for (int s0 = 0; s0 < width; s0 += kStep * kBatch) {
-    uint4 wv[kBatch][NMAT];
 #pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const int col = s0 + q * kStep + 16 * t;
-      const bool ok = row_ok && col < width;
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) wv[q][m] = ok ? ld16_ro_stream(wr[m] + col) : make_uint4(0, 0, 0, 0);
+  for (int q = 0; q < kSteps; ++q) {
+    const int c0 = cbase + q * kStep;
+    if (q * kStep >= P.cw || c0 >= cend) break;
+    uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
+    if (lane < 4 && c0 + 16 * t < cend) {
+      const uint32_t a = xs0 + 2u * uint32_t(c0 + 16 * t);
+      xa = ld_shared128(a);
+      xb = ld_shared128(a + 16u);
     }
+    const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
-    for (int q = 0; q < kBatch; ++q) {
-      const int c0 = s0 + q * kStep;
-      if (c0 >= width) break;
-      uint4 xa = make_uint4(0, 0, 0, 0), xb = xa;
-      if (lane < 4 && c0 + 16 * t < width) {
-        const uint32_t a = xs0 + 2u * uint32_t(cbase + c0 + 16 * t);
-        xa = ld_shared128(a);
-        xb = ld_shared128(a + 16u);
-      }
-      const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+    for (int i = 0; i < 4; ++i) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const uint32_t word = i == 0 ? wv[q][m].x : i == 1 ? wv[q][m].y : i == 2 ? wv[q][m].z : wv[q][m].w;
-          mma_16816(d[m], xw[2 * i], 0u, xw[2 * i + 1], 0u, e4m3x2_to_f16x2(word & 0xFFFFu),
-                    e4m3x2_to_f16x2(word >> 16));
-        }
+      for (int m = 0; m < NMAT; ++m) {
+        const uint32_t word = i == 0 ? wv[q][m].x : i == 1 ? wv[q][m].y : i == 2 ? wv[q][m].z : wv[q][m].w;
+        mma_16816(d[m], xw[2 * i], 0u, xw[2 * i + 1], 0u, e4m3x2_to_f16x2(word & 0xFFFFu),
+                  e4m3x2_to_f16x2(word >> 16));
       }
     }
   }
 }
 
-// Standalone single / dual GEMV: each warp owns whole 8-row blocks and adds
-// the pieces of a row in piece order in registers.
+// The units [u0, u1) of one phase for this CTA.  Loads of unit u+1 are in
+// flight while unit u is multiplied and reduced.  SPLIT: units are (block,
+// piece) pairs whose piece sums go to P.partial and the CTA adding a block's
+// last piece finishes the block; otherwise this CTA owns whole blocks and
+// sums their pieces in order itself.
+template <int NMAT, bool SPLIT>
+QFFN_DEVI void run_units(const Phase& P, int u0, int u1, uint32_t xs0, float down, float* red) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t = lane & 3;
+  uint4 wa[kSteps][NMAT], wb[kSteps][NMAT];
+  float acc = 0.0f;                      // finishing threads: running sum over pieces
+  if (u0 < u1) load_unit<NMAT>(P, unit_of(P, u0), warp, lane, wa);
+  auto finish = [&](int u, const uint4 (&cur)[kSteps][NMAT]) {
+    const Unit un = unit_of(P, u);
+    float d[2][4];
+    mma_unit<NMAT>(P, un, warp, lane, xs0, cur, d);
+    float* rb = red + (u & 1) * (2 * kWarps * kBlockRows);
+    if (lane < 4) {
+#pragma unroll
+      for (int m = 0; m < NMAT; ++m) {
+        rb[(m * kWarps + warp) * kBlockRows + 2 * t] = d[m][0];
+        rb[(m * kWarps + warp) * kBlockRows + 2 * t + 1] = d[m][1];
+      }
+    }
+    __syncthreads();
+    if (tid < kBlockRows * NMAT) {
+      const int m = tid / kBlockRows, r = tid % kBlockRows;
+      const int row = un.b * kBlockRows + r;
+      float pj = 0.0f;
+      for (int w = 0; w < kWarps; ++w) pj += rb[(m * kWarps + w) * kBlockRows + r];
+      if (SPLIT) {
+        if (row < P.rows) P.partial[(size_t(m) * P.pieces + un.j) * P.rows + row] = pj;
+      } else {
+        acc = un.j == 0 ? pj : acc + pj;
+        if (un.j == P.pieces - 1 && row < P.rows)
+          P.out[m][row] = f32_to_bf16(P.s[m][row] * (acc * down));
+      }
+    }
+    if (SPLIT && warp == 0) {
+      // publish this piece (release) and learn whether it was the block's last
+      // (acquire); the warp barrier orders lanes 1..7's writes before lane 0's
+      __syncwarp();
+      unsigned int done = 0;
+      if (lane == 0) done = atomic_add_acq_rel(P.done + un.b, 1u);
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (done == unsigned(P.pieces - 1) && lane < kBlockRows * NMAT) {
+        const int m = lane / kBlockRows, row = un.b * kBlockRows + lane % kBlockRows;
+        if (row < P.rows) {
+          float s = 0.0f;
+          for (int jj = 0; jj < P.pieces; ++jj) {
+            const float v = ld_cg_f32(P.partial + (size_t(m) * P.pieces + jj) * P.rows + row);
+            s = jj == 0 ? v : s + v;
+          }
+          P.out[m][row] = f32_to_bf16(P.s[m][row] * (s * down));
+        }
+      }
+    }
+  };
+  for (int u = u0; u < u1; u += 2) {
+    if (u + 1 < u1) load_unit<NMAT>(P, unit_of(P, u + 1), warp, lane, wb);
+    finish(u, wa);
+    if (u + 1 < u1) {
+      if (u + 2 < u1) load_unit<NMAT>(P, unit_of(P, u + 2), warp, lane, wa);
+      finish(u + 1, wb);
+    }
+  }
+}
+
+// contiguous share [u0, u1) of `n` units for this CTA
+QFFN_DEVI void cta_range(int n, int& u0, int& u1) {
+  u0 = int((int64_t(n) * blockIdx.x) / gridDim.x);
+  u1 = int((int64_t(n) * (blockIdx.x + 1)) / gridDim.x);
+}
+
+// Standalone single / dual GEMV: each CTA owns whole 8-row blocks.
 template <int NMAT>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const Phase P, const uint16_t* x) {
   extern __shared__ uint16_t xs[];
   __shared__ float xmax[kWarps];
+  __shared__ float red[2 * 2 * kWarps * kBlockRows];
   const float down = stage_x<false>(xs, x, nullptr, nullptr, P.cols, xmax);
   const uint32_t xs0 = uint32_t(__cvta_generic_to_shared(xs));
-  const int lane = threadIdx.x & 31;
-  const int nw = gridDim.x * kWarps;
-  for (int b = blockIdx.x * kWarps + (threadIdx.x >> 5); b < P.nblocks; b += nw) {
-    float tot[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
-    for (int j = 0; j < P.pieces; ++j) {
-      float d[2][4];
-      piece_partial<NMAT>(P, b, j, xs0, lane, d);
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        tot[m][0] = j == 0 ? d[m][0] : tot[m][0] + d[m][0];
-        tot[m][1] = j == 0 ? d[m][1] : tot[m][1] + d[m][1];
-      }
-    }
-    if (lane < 4) {
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = b * kBlockRows + 2 * lane + e;
-          if (row < P.rows) P.out[m][row] = f32_to_bf16(P.s[m][row] * (tot[m][e] * down));
-        }
-    }
-  }
-}
-
-// Fused decode phase body: units (block, piece) spread over all warps; piece
-// partials to global memory; the warp that finishes a block's last piece adds
-// the block's pieces in order and writes its rows.
-template <int NMAT>
-QFFN_DEVI void fused_phase(const Phase& P, uint32_t xs0, float down) {
-  const int lane = threadIdx.x & 31;
-  const int nw = gridDim.x * kWarps;
-  const int units = P.nblocks * P.pieces;
-  for (int un = blockIdx.x * kWarps + (threadIdx.x >> 5); un < units; un += nw) {
-    const int b = un / P.pieces, j = un % P.pieces;
-    float d[2][4];
-    piece_partial<NMAT>(P, b, j, xs0, lane, d);
-    if (lane < 4) {
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int row = b * kBlockRows + 2 * lane + e;
-          if (row < P.rows) P.partial[(size_t(m) * P.pieces + j) * P.rows + row] = d[m][e];
-        }
-    }
-    // publish this piece (release) and learn whether it was the block's last
-    // (acquire): the warp barrier orders the other lanes' writes before lane 0
-    __syncwarp();
-    unsigned int done = 0;
-    if (lane == 0) done = atomic_add_acq_rel(P.done + b, 1u);
-    done = __shfl_sync(0xffffffffu, done, 0);
-    if (done == unsigned(P.pieces - 1)) {
-      if (lane < kBlockRows * NMAT) {
-        const int m = lane / kBlockRows, row = b * kBlockRows + lane % kBlockRows;
-        if (row < P.rows) {
-          float t = 0.0f;
-          for (int jj = 0; jj < P.pieces; ++jj) {
-            const float v = ld_cg_f32(P.partial + (size_t(m) * P.pieces + jj) * P.rows + row);
-            t = jj == 0 ? v : t + v;
-          }
-          P.out[m][row] = f32_to_bf16(P.s[m][row] * (t * down));
-        }
-      }
-    }
-  }
+  int b0, b1;
+  cta_range(P.nblocks, b0, b1);
+  run_units<NMAT, false>(P, b0 * P.pieces, b1 * P.pieces, xs0, down, red);
 }
 
 __global__ void __launch_bounds__(kThreads) decode_fused_kernel(const Params p) {
   extern __shared__ uint16_t xs[];
   __shared__ float xmax[kWarps];
+  __shared__ float red[2 * 2 * kWarps * kBlockRows];
   __shared__ int s_abort;
   const uint32_t xs0 = uint32_t(__cvta_generic_to_shared(xs));
-  // phase 0: g, u = dual GEMV of x
+  // phase 0: g, u = dual GEMV of x (whole blocks per CTA)
   float down = stage_x<false>(xs, p.x, nullptr, nullptr, p.ph[0].cols, xmax);
-  fused_phase<2>(p.ph[0], xs0, down);
+  int u0, u1;
+  cta_range(p.ph[0].nblocks, u0, u1);
+  run_units<2, false>(p.ph[0], u0 * p.ph[0].pieces, u1 * p.ph[0].pieces, xs0, down, red);
   // grid-wide barrier: every CTA has written its g and u rows
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -297,16 +322,19 @@ __global__ void __launch_bounds__(kThreads) decode_fused_kernel(const Params p) 
   }
   __syncthreads();
   if (s_abort) return;            // uniform across the CTA
-  // phase 1: out = down GEMV of h = bf16(silu(g) * u)
+  // phase 1: out = down GEMV of h = bf16(silu(g) * u), (block, piece) units over CTAs
   down = stage_x<true>(xs, nullptr, p.g, p.u, p.ph[1].cols, xmax);
-  fused_phase<1>(p.ph[1], xs0, down);
+  cta_range(p.ph[1].nblocks * p.ph[1].pieces, u0, u1);
+  run_units<1, true>(p.ph[1], u0, u1, xs0, down, red);
 }
 
 void set_phase(Phase& P, int rows, int cols, int nmat) {
   P.rows = rows;
   P.cols = cols;
   P.nmat = nmat;
-  P.pieces = (cols + kPiece - 1) / kPiece;
+  P.pieces = (cols + kPieceMax - 1) / kPieceMax;
+  P.piece = ((cols + P.pieces - 1) / P.pieces + kStep - 1) / kStep * kStep;
+  P.cw = ((P.piece + kWarps - 1) / kWarps + kStep - 1) / kStep * kStep;
   P.nblocks = (rows + kBlockRows - 1) / kBlockRows;
 }
 
@@ -317,15 +345,14 @@ cudaError_t set_smem_attr(const void* fn, size_t smem) {
 
 }  // namespace
 
-size_t decode_counter_bytes(int64_t C, int64_t H) {
-  // grid barrier, then pieces done per 8-row block of g/u and of out
-  return (size_t(1) + size_t((H + kBlockRows - 1) / kBlockRows) + size_t((C + kBlockRows - 1) / kBlockRows)) *
-         sizeof(unsigned int);
+size_t decode_counter_bytes(int64_t C, int64_t /*H*/) {
+  // grid barrier, then pieces done per 8-row block of out
+  return (size_t(1) + size_t((C + kBlockRows - 1) / kBlockRows)) * sizeof(unsigned int);
 }
 
 size_t decode_partial_bytes(int64_t C, int64_t H) {
-  return (size_t(2) * size_t((C + kPiece - 1) / kPiece) * size_t(H) +
-          size_t((H + kPiece - 1) / kPiece) * size_t(C)) * sizeof(float);
+  // piece sums of the down projection: one per K piece of h per output row
+  return size_t((H + kPieceMax - 1) / kPieceMax) * size_t(C) * sizeof(float);
 }
 
 cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const uint8_t* w0,
@@ -373,15 +400,13 @@ cudaError_t launch_decode_fused(uint16_t* out, const uint16_t* x, const uint8_t*
   A.s[1] = s_up;
   A.out[1] = u;
   set_phase(A, int(H), int(C), 2);
-  A.done = counter + 1;
-  A.partial = partial;
   Phase& D = p.ph[1];
   D.w[0] = w_down;
   D.s[0] = s_down;
   D.out[0] = out;
   set_phase(D, int(C), int(H), 1);
-  D.done = counter + 1 + A.nblocks;
-  D.partial = partial + size_t(2) * A.pieces * size_t(H);
+  D.done = counter + 1;
+  D.partial = partial;
   p.x = x;
   p.g = g;
   p.u = u;

@@ -24,18 +24,16 @@
 namespace {
 
 // Largest sizes this entry point accepts, and its scratch: g and u (H bf16
-// each), the decode kernel's counters (grid barrier, one per 8-row block of
-// g/u and of the output) and its fp32 partial sums (one per 512-column piece
-// per row of g, u and the output).
+// each), the decode kernel's counters (grid barrier and one per 8-row block
+// of the output) and its fp32 partial sums (one per 4096-column piece of h per
+// output row).
 constexpr int64_t kNoAllocMaxH = 32768;
 constexpr int64_t kNoAllocMaxC = 8192;
 constexpr size_t kScratchG = 0;
 constexpr size_t kScratchU = size_t(kNoAllocMaxH) * 2;
 constexpr size_t kScratchCounter = 2 * kScratchU;
-constexpr size_t kScratchPartial =
-    kScratchCounter + ((4 * (1 + kNoAllocMaxH / 8 + kNoAllocMaxC / 8) + 255) / 256) * 256;
-constexpr size_t kScratchBytes =
-    kScratchPartial + 4 * (2 * (kNoAllocMaxC / 512) * kNoAllocMaxH + (kNoAllocMaxH / 512) * kNoAllocMaxC);
+constexpr size_t kScratchPartial = kScratchCounter + ((4 * (1 + kNoAllocMaxC / 8) + 255) / 256) * 256;
+constexpr size_t kScratchBytes = kScratchPartial + 4 * (kNoAllocMaxH / 4096) * kNoAllocMaxC;
 
 static __device__ __align__(256) uint8_t g_decode_scratch[kScratchBytes];
 
