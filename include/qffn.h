@@ -188,10 +188,10 @@ qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream
  * normalised), Wg, Wu [H, C] E4M3 with s_gate, s_up [H]; Wd [C, H] E4M3 with
  * s_down [C]; out [C] bf16.  workspace >= qffn_decode_workspace_size() bytes,
  * 16-byte aligned: g [H] bf16 at offset 0 and u [H] bf16 at offset
- * round_up(2H, 256) (both readable after the call), then counters the call
- * zeroes and fp32 partial sums.  Runs as one cooperative launch (gate/up
- * GEMV, grid barrier, down GEMV on h = bf16(silu(g) * u)); bit-identical to
- * qffn_gemv_dual, qffn_silu_mul, qffn_gemv.
+ * round_up(2H, 256), both readable after the call.  Two launches: the dual
+ * gate/up GEMV, then the down GEMV, which forms h = bf16(silu(g) * u) in its
+ * prologue (silu_mul folded in) and starts as a programmatic dependent launch;
+ * bit-identical to qffn_gemv_dual, qffn_silu_mul, qffn_gemv.
  * C % 16 == 0, H % 16 == 0, 16 <= C, H <= 32768. */
 size_t qffn_decode_workspace_size(int64_t C, int64_t H);
 qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
@@ -205,20 +205,18 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
  * not permitted, such as a plugin's enqueue step or a host callback, or a
  * process whose device memory is all owned by another allocator) and so
  * cannot supply the workspace of qffn_decode_forward.
- * Computes exactly what qffn_decode_forward computes (same kernel, same
- * bits), with its scratch (the g and u vectors, counters and fp32 partial
- * sums of the down projection) in a fixed array inside the library:
- * 388 KiB per GPU that loads the library, held until the process exits.
- * H > 32768 or C > 8192 is rejected with QFFN_ERR_UNSUPPORTED_SHAPE; the other
- * size and alignment rules are those of qffn_decode_forward.  Nothing is
- * allocated by this call.
+ * Computes exactly what qffn_decode_forward computes (same kernels, same
+ * bits), with its scratch (the g and u vectors) in a fixed array inside the
+ * library: 2 x 32768 bf16 (128 KiB) per GPU that loads the library, held
+ * until the process exits.  H > 32768 is rejected with
+ * QFFN_ERR_UNSUPPORTED_SHAPE; the other size and alignment rules are those of
+ * qffn_decode_forward.  Nothing is allocated by this call.
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
  * All calls on a device share the array and it keeps the last call's
- * contents (g, u and the partial sums are written before they are read; the
- * counters are cleared on the stream at the start of every call).  Calls
- * that overlap in time on the GPU race on the array: order them on one
- * stream or with events. */
+ * contents (g and u are written before they are read, so nothing needs
+ * clearing).  Calls that overlap in time on the GPU race on the array: order
+ * them on one stream or with events. */
 qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
                                         const float* s_gate, const uint8_t* w_up,
                                         const float* s_up, const uint8_t* w_down,

@@ -44,12 +44,10 @@ void forward_offsets(int64_t N, int64_t C, int64_t H, size_t off[5]) {
   off[4] = round_up(off[3] + size_t(N) * size_t(H), 256);
 }
 
-// decode workspace: g [H] bf16 | u [H] bf16 | counters | fp32 partial sums, each 256-byte aligned
-void decode_offsets(int64_t C, int64_t H, size_t off[4]) {
-  off[0] = round_up(size_t(H) * 2, 256);                         // u
-  off[1] = 2 * off[0];                                          // counters
-  off[2] = off[1] + round_up(qffn::decode_counter_bytes(C, H), 256);  // partials
-  off[3] = off[2] + round_up(qffn::decode_partial_bytes(C, H), 256);
+// decode workspace: g [H] bf16 | u [H] bf16, each 256-byte aligned
+void decode_offsets(int64_t H, size_t off[2]) {
+  off[0] = round_up(size_t(H) * 2, 256);   // u
+  off[1] = 2 * off[0];                     // end
 }
 
 qffn_status check_forward_shape(int64_t B, int64_t T, int64_t C, int64_t H) {
@@ -255,9 +253,9 @@ qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream
 
 size_t qffn_decode_workspace_size(int64_t C, int64_t H) {
   if (C < 16 || H < 16 || C > 32768 || H > 32768) return 0;
-  size_t off[4];
-  decode_offsets(C, H, off);
-  return off[3];
+  size_t off[2];
+  decode_offsets(H, off);
+  return off[1];
 }
 
 qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
@@ -273,15 +271,13 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
   QFFN_ALIGNED4(s_gate); QFFN_ALIGNED4(s_up); QFFN_ALIGNED4(s_down);
   QFFN_ALIGNED(workspace);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  size_t off[4];
-  decode_offsets(C, H, off);
+  size_t off[2];
+  decode_offsets(H, off);
   uint16_t* g = reinterpret_cast<uint16_t*>(ws);
   uint16_t* u = reinterpret_cast<uint16_t*>(ws + off[0]);
-  unsigned int* counter = reinterpret_cast<unsigned int*>(ws + off[1]);
-  float* partial = reinterpret_cast<float*>(ws + off[2]);
-  // A6, A7 and A8 in one cooperative launch (see decode.cu)
-  return from_cuda(qffn::launch_decode_fused(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C,
-                                             H, g, u, counter, partial, stream));
+  // A6, then A7 folded into A8 (see decode.cu)
+  return from_cuda(qffn::launch_decode(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, g,
+                                       u, stream));
 }
 
 }  // extern "C"

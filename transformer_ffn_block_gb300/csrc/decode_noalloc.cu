@@ -11,9 +11,8 @@
 //
 // The scratch array below lives in every GPU that loads the library, for as
 // long as the process runs.  All calls on a device share it and it keeps what
-// the last call wrote; the decode writes every g/u element and partial sum
-// before reading it, and the counters that must start at zero are cleared on
-// the stream at the start of every call.  Calls whose
+// the last call wrote; the decode writes every g/u element before reading
+// it, so nothing needs clearing between calls.  Calls whose
 // execution overlaps on the GPU (different streams, no ordering between them)
 // use the same array and race; order them on one stream or with events.
 #include <mutex>
@@ -23,17 +22,12 @@
 
 namespace {
 
-// Largest sizes this entry point accepts, and its scratch: g and u (H bf16
-// each), the decode kernel's counters (grid barrier and one per 8-row block
-// of the output) and its fp32 partial sums (one per 4096-column piece of h per
-// output row).
+// Largest sizes this entry point accepts, and its scratch: g and u, H bf16 each.
 constexpr int64_t kNoAllocMaxH = 32768;
-constexpr int64_t kNoAllocMaxC = 8192;
+constexpr int64_t kNoAllocMaxC = 32768;
 constexpr size_t kScratchG = 0;
 constexpr size_t kScratchU = size_t(kNoAllocMaxH) * 2;
-constexpr size_t kScratchCounter = 2 * kScratchU;
-constexpr size_t kScratchPartial = kScratchCounter + ((4 * (1 + kNoAllocMaxC / 8) + 255) / 256) * 256;
-constexpr size_t kScratchBytes = kScratchPartial + 4 * (kNoAllocMaxH / 4096) * kNoAllocMaxC;
+constexpr size_t kScratchBytes = 2 * kScratchU;
 
 static __device__ __align__(256) uint8_t g_decode_scratch[kScratchBytes];
 
@@ -80,11 +74,9 @@ extern "C" qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t
   if (scratch_address(&scratch) != cudaSuccess) return QFFN_ERR_CUDA;
   uint16_t* g = reinterpret_cast<uint16_t*>(scratch + kScratchG);
   uint16_t* u = reinterpret_cast<uint16_t*>(scratch + kScratchU);
-  unsigned int* counter = reinterpret_cast<unsigned int*>(scratch + kScratchCounter);
-  float* partial = reinterpret_cast<float*>(scratch + kScratchPartial);
-  // the same launch as qffn_decode_forward, with the scratch array as workspace
-  if (qffn::launch_decode_fused(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, g, u,
-                                counter, partial, stream) != cudaSuccess)
+  // the same launches as qffn_decode_forward, with the scratch array as workspace
+  if (qffn::launch_decode(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, g, u, stream) !=
+      cudaSuccess)
     return QFFN_ERR_CUDA;
   return QFFN_OK;
 }

@@ -47,19 +47,14 @@ cudaError_t gemm_take_status(unsigned int* status);
 cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const uint8_t* w0,
                         const float* s0, const uint8_t* w1, const float* s1, int64_t rows,
                         int64_t cols, bool pdl, cudaStream_t s);
-// The whole decode FFN in one cooperative launch: g, u = dual GEMV of x (written
-// to g, u), grid barrier on counter[0], out = down GEMV of bf16(silu(g) * u);
-// work units spread over all warps with piece partials in `partial`.  Same bits as
-// launch_gemv + launch_silu_mul + launch_gemv.
-// counter: decode_counter_bytes(C, H) bytes (zeroed here); partial:
-// decode_partial_bytes(C, H) bytes of fp32 scratch.
-cudaError_t launch_decode_fused(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
-                                const float* s_gate, const uint8_t* w_up, const float* s_up,
-                                const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
-                                uint16_t* g, uint16_t* u, unsigned int* counter, float* partial,
-                                cudaStream_t s);
-size_t decode_counter_bytes(int64_t C, int64_t H);
-size_t decode_partial_bytes(int64_t C, int64_t H);
+// The whole decode FFN: the dual GEMV (g, u), then the down GEMV on
+// h = bf16(silu(g) * u) formed in its prologue, launched as a programmatic
+// dependent launch so its first weight loads overlap the dual GEMV's tail.
+// Same bits as launch_gemv + launch_silu_mul + launch_gemv.
+cudaError_t launch_decode(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
+                          const float* s_gate, const uint8_t* w_up, const float* s_up,
+                          const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
+                          uint16_t* g, uint16_t* u, cudaStream_t s);
 // Reads and clears the decode kernels' device status word of the current device.
 cudaError_t decode_take_status(unsigned int* status);
 
