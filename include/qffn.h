@@ -187,11 +187,12 @@ qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream
  * [metrale] DenseFfnLayer::forward, FP8 split-SiLU arm.  x [C] bf16 (already
  * normalised), Wg, Wu [H, C] E4M3 with s_gate, s_up [H]; Wd [C, H] E4M3 with
  * s_down [C]; out [C] bf16.  workspace >= qffn_decode_workspace_size() bytes,
- * 16-byte aligned: g [H] bf16 at offset 0 and u [H] bf16 at offset
- * round_up(2H, 256), both readable after the call.  Two launches: the dual
- * gate/up GEMV, then the down GEMV, which forms h = bf16(silu(g) * u) in its
- * prologue (silu_mul folded in) and starts as a programmatic dependent launch;
- * bit-identical to qffn_gemv_dual, qffn_silu_mul, qffn_gemv.
+ * 16-byte aligned.  After the call it holds, as the split-SiLU arm leaves
+ * its buffers, h = bf16(silu(g) * u) [H] bf16 at offset 0 (the gate buffer)
+ * and u [H] bf16 at offset round_up(2H, 256).  Two launches: the dual gate/up
+ * GEMV with silu_mul applied as g and u are produced, then the down GEMV as a
+ * programmatic dependent launch; bit-identical to qffn_gemv_dual,
+ * qffn_silu_mul, qffn_gemv.
  * C % 16 == 0, H % 16 == 0, 16 <= C, H <= 32768. */
 size_t qffn_decode_workspace_size(int64_t C, int64_t H);
 qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,

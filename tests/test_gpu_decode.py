@@ -45,27 +45,30 @@ def test_decode_forward(q, C, H):
         np.testing.assert_array_equal(host(recs[k][1]), ref_rec[k][1])
     ref = oracle.decode_forward(di["x"], *ref_rec["w_gate"], *ref_rec["w_up"], *ref_rec["w_down"])
     assert_out_close(bf(out), ref["out"])
-    # stage-wise: g and u (left in the workspace) against the exact dual GEMV, and
-    # out against the exact down GEMV of silu_mul of the GPU's own g, u
-    vec = (2 * cfg.H + 255) // 256 * 256
-    gb = bf(ws[:2 * cfg.H].view(torch.int16))
-    ub = bf(ws[vec:vec + 2 * cfg.H].view(torch.int16))
-    xa = np.abs(oracle.bf16_to_f64(di["x"]))
-    for got, want, (wq, ws_) in ((gb, ref["g"], ref_rec["w_gate"]), (ub, ref["u"], ref_rec["w_up"])):
-        absdot = (np.abs(oracle.e4m3_decode(wq)) @ xa) * ws_.astype(np.float64)
-        check_dot_outputs(got, want, absdot, cfg.C, max_mismatch=0.02)
-    h_gpu = oracle.silu_mul(gb, ub)
-    out_stage = oracle.gemv_row_scaled(h_gpu, *ref_rec["w_down"])
-    absdot = (np.abs(oracle.e4m3_decode(ref_rec["w_down"][0])) @ np.abs(oracle.bf16_to_f64(h_gpu))) \
-        * ref_rec["w_down"][1].astype(np.float64)
-    check_dot_outputs(bf(out), out_stage, absdot, cfg.H, max_mismatch=0.02)
-    # the dual entry point writes the same g, u bits
+    # stage-wise: g and u from the dual entry point against the exact dual GEMV;
+    # the workspace holds h (gate buffer) and u as the split-SiLU arm leaves them
     g = empty_bf16(cfg.H)
     u = empty_bf16(cfg.H)
     q.qffn_gemv_dual(g, u, x, *recs["w_gate"], *recs["w_up"], cfg.H, cfg.C)
     sync()
-    np.testing.assert_array_equal(bf(g), gb)
-    np.testing.assert_array_equal(bf(u), ub)
+    gb, ub = bf(g), bf(u)
+    xa = np.abs(oracle.bf16_to_f64(di["x"]))
+    for got, want, (wq, ws_) in ((gb, ref["g"], ref_rec["w_gate"]), (ub, ref["u"], ref_rec["w_up"])):
+        absdot = (np.abs(oracle.e4m3_decode(wq)) @ xa) * ws_.astype(np.float64)
+        check_dot_outputs(got, want, absdot, cfg.C, max_mismatch=0.02)
+    vec = (2 * cfg.H + 255) // 256 * 256
+    h_ws = bf(ws[:2 * cfg.H].view(torch.int16))
+    np.testing.assert_array_equal(bf(ws[vec:vec + 2 * cfg.H].view(torch.int16)), ub)
+    assert bf16_ulp_diff(h_ws, oracle.silu_mul(gb, ub)).max() <= 1
+    out_stage = oracle.gemv_row_scaled(h_ws, *ref_rec["w_down"])
+    absdot = (np.abs(oracle.e4m3_decode(ref_rec["w_down"][0])) @ np.abs(oracle.bf16_to_f64(h_ws))) \
+        * ref_rec["w_down"][1].astype(np.float64)
+    check_dot_outputs(bf(out), out_stage, absdot, cfg.H, max_mismatch=0.02)
+    # h in the workspace is exactly what the silu_mul entry point makes of g, u
+    g2 = g.clone()
+    q.qffn_silu_mul(g2, u, cfg.H)
+    sync()
+    np.testing.assert_array_equal(bf(g2), h_ws)
 
 
 def test_decode_per_projection_arm_bit_identical(q):

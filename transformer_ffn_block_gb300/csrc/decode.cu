@@ -4,271 +4,163 @@
 //
 //   out[r] = bf16(row_scale[r] * sum_k W[r,k] * x[k]),  W E4M3, x bf16.
 //
-// A warp owns 8-row blocks.  It streams them through a private shared-memory
-// ring with 16-byte asynchronous copies (cp.async: row-contiguous 512-byte
-// spans per copy instruction, nothing held in registers while in flight),
-// several 256-column stages ahead, and multiplies each stage with warp-level
-// tensor-core MMAs (m16n8k16, f16 inputs, fp32 accumulation): the 8 rows are
-// the 8 columns of the B operand (E4M3 -> f16 is exact; a 16-byte row pitch
-// pad makes the fragment reads conflict-free), x is row 0 of the A operand.
-// x enters as f16 after an exact power-of-two scaling 2^k chosen from max|x|
-// (every x with |x| >= max|x| 2^-29 is exact in f16, nothing overflows);
-// 2^-k is applied to the finished sum.  Rows longer than 4096 columns are
-// split over a team of 2, 4 or 8 warps (K parts) whose sums the team leader
-// adds in part order.
+// A team of TPR threads owns a row at a time: thread t holds the 16-byte
+// chunks t, t+TPR, ... of the row and issues all of its loads (16-byte,
+// non-allocating, one contiguous 16*TPR-byte span per load instruction)
+// before using any, so every thread keeps the whole row in flight.  x sits
+// in shared memory as bf16.  Products and sums are packed fp32x2 fmas: the
+// E4M3 pairs go through the e4m3x2 -> f16x2 convert to float pairs, x pairs
+// are widened from bf16 by shifts; even elements accumulate in the low half
+// and odd ones in the high half.  The per-row arithmetic (chunk order, pair
+// order, halves added, warp butterfly, warps of a team in order) is the same
+// code for the single and the dual form, so they agree bit for bit; the dual
+// form reads x once for the gate and the up row of the same index.
 //
-// Per row the arithmetic depends only on the row length, so the single and
-// dual GEMVs agree bit for bit, and so does the down GEMV that forms its own
-// input h = bf16(silu(g) * u) (the decode's silu_mul folded into its
-// prologue).  That kernel is a programmatic dependent launch: its first weight
-// stages are in flight before it waits for the dual GEMV's g and u.
-#include <cuda_fp16.h>
-
+// In the decode the dual GEMV applies silu_mul where g and u are produced and
+// leaves h = bf16(silu(g) * u) in the gate buffer (the split-SiLU arm's
+// buffer use); the down GEMV on h is a programmatic dependent launch whose
+// CTAs start as the dual GEMV's CTAs retire and wait for h only right before
+// reading it.
 #include "common.cuh"
 #include "launch.h"
-#include "pipeline.cuh"
 
 namespace qffn {
 namespace {
 
-constexpr int kWarps = 12;
-constexpr int kThreads = kWarps * 32;
-constexpr int kBlockRows = 8;              // rows per MMA (the n8 of m16n8k16)
-constexpr int kSeg = 256;                  // columns per ring stage
-constexpr int kPitch = kSeg + 16;          // bytes per row in a stage (bank-conflict pad)
-constexpr int kMatStage = kBlockRows * kPitch;
-constexpr int kPartMax = 4096;             // columns per K part at most
-constexpr int kSmemBudget = 226 * 1024;
+constexpr int kThreads = 256;
+constexpr int kU = 8;
+
+QFFN_DEVI uint64_t e4m3x2_to_f2(uint32_t two_codes) {
+  uint32_t h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(uint16_t(two_codes)));
+  const float2 f = __half22float2(*reinterpret_cast<__half2*>(&h));
+  return f2_pack(f.x, f.y);
+}
+
+// acc += the 16 products of one weight chunk with its 16 x values (x as 16
+// bf16 in two uint4), element pairs in order.
+QFFN_DEVI void dot16(uint4 w, uint4 xa, uint4 xb, uint64_t& acc) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    acc = f2_fma(e4m3x2_to_f2(ww[j] & 0xFFFFu), bf16x2_to_f2(xw[2 * j]), acc);
+    acc = f2_fma(e4m3x2_to_f2(ww[j] >> 16), bf16x2_to_f2(xw[2 * j + 1]), acc);
+  }
+}
 
 struct Gemv {
   uint16_t* out[2];
-  const uint16_t* x;         // input bf16 [cols], or with SILU: g
-  const uint16_t* u;         // SILU: up values
+  const uint16_t* x;         // input bf16 [cols]
   const uint8_t* w[2];
   const float* s[2];
   int rows, cols;
-  int team, kpart;           // warps per block and columns per warp (multiple of 16)
-  int nstage;                // ring stages per warp
 };
 
-QFFN_DEVI void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-QFFN_DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-QFFN_DEVI void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-QFFN_DEVI void cp_async_wait_dyn(int n) {   // at most n of this thread's groups still pending
-  switch (n) {
-    case 0: cp_async_wait<0>(); break;
-    case 1: cp_async_wait<1>(); break;
-    case 2: cp_async_wait<2>(); break;
-    case 3: cp_async_wait<3>(); break;
-    case 4: cp_async_wait<4>(); break;
-    case 5: cp_async_wait<5>(); break;
-    case 6: cp_async_wait<6>(); break;
-    default: cp_async_wait<7>(); break;
-  }
-}
-QFFN_DEVI uint32_t ld_shared32(uint32_t addr) {
-  uint32_t r;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(r) : "r"(addr));
-  return r;
-}
-QFFN_DEVI uint2 ld_shared64(uint32_t addr) {
-  uint2 r;
-  asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "r"(addr));
-  return r;
-}
-QFFN_DEVI uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(uint16_t(two_codes)));
-  return r;
-}
-// D += A(16x16, f16, row) * B(16x8, f16, col), fp32 accumulate
-QFFN_DEVI void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9},"
-      " {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
-}
-
-// x (or h = bf16(silu(g) * u)) into shared memory as f16 scaled by 2^k, by
-// the whole CTA; returns 2^-k.
-template <bool SILU>
-QFFN_DEVI float stage_x(uint16_t* xs, const Gemv& G, float* xmax) {
-  const int tid = threadIdx.x;
-  float m = 0.0f;
-  for (int c = tid; c < (G.cols >> 3); c += kThreads) {
-    uint4 v;
-    if (SILU) v = swiglu8(ld16_once(G.x + size_t(c) * 8), ld16_once(G.u + size_t(c) * 8));
-    else v = ld16_once(G.x + size_t(c) * 8);
-    *reinterpret_cast<uint4*>(xs + size_t(c) * 8) = v;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
-  }
-  m = warp_max(m);
-  if ((tid & 31) == 0) xmax[tid >> 5] = m;
-  __syncthreads();
-  float amax = 0.0f;
-  for (int w = 0; w < kWarps; ++w) amax = fmaxf(amax, xmax[w]);
-  int e = 0;
-  frexpf(amax, &e);                                   // amax = f * 2^e, f in [0.5, 1)
-  const int k = amax > 0.0f ? 15 - e : 0;             // amax * 2^k in [2^14, 2^15)
-  const float up = ldexpf(1.0f, k);
-  for (int c = tid; c < (G.cols >> 3); c += kThreads) {
-    const uint4 v = *reinterpret_cast<uint4*>(xs + size_t(c) * 8);
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __half2 h = __floats2half2_rn(bf16_lo(w[j]) * up, bf16_hi(w[j]) * up);
-      w[j] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(xs + size_t(c) * 8) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-  __syncthreads();
-  return ldexpf(1.0f, -k);
-}
-
-template <int NMAT, bool SILU>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Gemv G) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);
-  uint8_t* rings = smem + ((size_t(G.cols) * 2 + 127) / 128) * 128;
-  __shared__ float xmax[kWarps];
+// SILU (dual only): the gate output slot receives h = bf16(silu(g) * u)
+// instead of g -- the decode's silu_mul applied where g and u are produced,
+// as the split-SiLU arm leaves h in the gate buffer.
+template <bool DUAL, bool SILU, int TPR>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
+  extern __shared__ uint4 xs[];
+  __shared__ float red[2][kThreads / 32];
+  constexpr int RPB = kThreads / TPR;   // rows per block step
+  constexpr int WPR = TPR / 32;         // warps per row
+  const int rows = G.rows, cols = G.cols;
+  const int nvec = cols >> 3;
+  const int nchunk = cols >> 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g8 = lane >> 2, t4 = lane & 3;
-  const int nteams = kWarps / G.team;
-  const int team = warp / G.team, part = warp % G.team;
-  const int k0 = part * G.kpart;
-  const int k1 = min(G.cols, k0 + G.kpart);
-  const int nseg = k1 > k0 ? (k1 - k0 + kSeg - 1) / kSeg : 0;
-  const int nblocks = (G.rows + kBlockRows - 1) / kBlockRows;
-  const int gteam = blockIdx.x * nteams + team, nteam_all = gridDim.x * nteams;
-  const bool active = team < nteams;            // warps left over when team does not divide 12
-  const int my_blocks = active && nblocks > gteam ? (nblocks - gteam + nteam_all - 1) / nteam_all : 0;
-  const int nstages = my_blocks * nseg;
-  const int stage_bytes = NMAT * kMatStage;
-  const uint32_t ring0 = uint32_t(__cvta_generic_to_shared(rings)) + uint32_t(warp * G.nstage * stage_bytes);
+  const int sub = threadIdx.x / TPR, t = threadIdx.x % TPR;
 
-  // stage i of this warp: block gteam + (i / nseg) * nteam_all, segment i % nseg
-  auto issue = [&](int i) {
-    if (i < nstages) {
-      const int b = gteam + (i / nseg) * nteam_all;
-      const int c0 = k0 + (i % nseg) * kSeg;
-      const int npiece = min(kSeg, k1 - c0) >> 4;
-      const int nr = min(kBlockRows, G.rows - b * kBlockRows);
-      const uint32_t dst = ring0 + uint32_t((i % G.nstage) * stage_bytes);
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m)
-        for (int q = lane; q < kBlockRows * (kSeg / 16); q += 32) {
-          const int r = q / (kSeg / 16), p = q % (kSeg / 16);
-          if (r < nr && p < npiece)
-            cp_async16(dst + uint32_t(m * kMatStage + r * kPitch + 16 * p),
-                       G.w[m] + size_t(b * kBlockRows + r) * G.cols + c0 + 16 * p);
-        }
-    }
-    cp_async_commit();               // (empty groups keep the counting uniform)
-  };
-  for (int i = 0; i < G.nstage - 1; ++i) issue(i);
-  if (SILU) pdl_wait();              // g and u come from the preceding kernel
+  pdl_wait();                        // x may come from the preceding kernel
   pdl_trigger();
-  const float down = stage_x<SILU>(xs, G, xmax);
-  const uint32_t xs0 = uint32_t(__cvta_generic_to_shared(xs));
+  for (int i = threadIdx.x; i < nvec; i += kThreads) xs[i] = ld16_once(G.x + size_t(i) * 8);
+  __syncthreads();
 
-  float d[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-  int blk = 0;
-  for (int i = 0; i < nstages; ++i) {
-    issue(i + G.nstage - 1);
-    cp_async_wait_dyn(G.nstage - 1);
-    __syncwarp();
-    const int seg = i % nseg;
-    const int c0 = k0 + seg * kSeg;
-    const int nstep = min(kSeg, k1 - c0) >> 4;
-    const uint32_t src = ring0 + uint32_t((i % G.nstage) * stage_bytes);
-    for (int st = 0; st < nstep; ++st) {
-      uint32_t a0 = 0u, a2 = 0u;
-      if (lane < 4) {
-        const uint2 xv = ld_shared64(xs0 + 2u * uint32_t(c0 + 16 * st + 4 * t4));
-        a0 = xv.x;
-        a2 = xv.y;
-      }
+  for (int base = blockIdx.x * RPB; base < rows; base += gridDim.x * RPB) {
+    const int row = base + sub;
+    uint64_t acc0 = 0ull, acc1 = 0ull;
+    if (row < rows) {
+      const uint8_t* r0 = G.w[0] + size_t(row) * size_t(cols);
+      const uint8_t* r1 = DUAL ? G.w[1] + size_t(row) * size_t(cols) : nullptr;
+      for (int c = t; c < nchunk; c += TPR * kU) {
+        uint4 a[kU], b[kU];
 #pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        const uint32_t wv = ld_shared32(src + uint32_t(m * kMatStage + g8 * kPitch + 16 * st + 4 * t4));
-        mma_16816(d[m], a0, a2, e4m3x2_to_f16x2(wv & 0xFFFFu), e4m3x2_to_f16x2(wv >> 16));
-      }
-    }
-    __syncwarp();                    // every lane is done with this ring slot
-    if (seg == nseg - 1) {
-      const int b = gteam + (i / nseg) * nteam_all;
-      // lanes 0..3 hold rows 8b + 2*lane (d[m][0]) and 8b + 2*lane + 1 (d[m][1])
-      float v[2][2];
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        v[m][0] = d[m][0];
-        v[m][1] = d[m][1];
-        d[m][0] = d[m][1] = d[m][2] = d[m][3] = 0.0f;
-      }
-      if (G.team == 1) {
-        if (lane < 4)
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int row = b * kBlockRows + 2 * lane + e;
-              if (row < G.rows) G.out[m][row] = f32_to_bf16(G.s[m][row] * (v[m][e] * down));
-            }
-      } else {
-        // team: every warp leaves its 8 row sums (per matrix) in shared memory
-        __shared__ float tred[2][kWarps][2][kBlockRows];
-        if (lane < 4)
-#pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-            tred[blk & 1][warp][m][2 * lane] = v[m][0];
-            tred[blk & 1][warp][m][2 * lane + 1] = v[m][1];
+        for (int u = 0; u < kU; ++u) {
+          const int cc = c + TPR * u;
+          if (cc < nchunk) {
+            a[u] = ld16_ro_stream(r0 + size_t(cc) * 16);
+            if (DUAL) b[u] = ld16_ro_stream(r1 + size_t(cc) * 16);
           }
-        named_sync(1 + team, G.team * 32);
-        if (part == 0 && lane < kBlockRows * NMAT) {
-          const int m = lane / kBlockRows, r = lane % kBlockRows;
-          const int row = b * kBlockRows + r;
-          float t = 0.0f;
-          for (int q = 0; q < G.team; ++q) t += tred[blk & 1][warp + q][m][r];
-          if (row < G.rows) G.out[m][row] = f32_to_bf16(G.s[m][row] * (t * down));
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int cc = c + TPR * u;
+          if (cc < nchunk) {
+            const uint4 xa = xs[2 * cc], xb = xs[2 * cc + 1];
+            dot16(a[u], xa, xb, acc0);
+            if (DUAL) dot16(b[u], xa, xb, acc1);
+          }
         }
       }
-      ++blk;
+    }
+    float s0, s1 = 0.0f;
+    {
+      float lo, hi;
+      f2_unpack(acc0, lo, hi);
+      s0 = warp_sum(lo + hi);
+      if (DUAL) {
+        f2_unpack(acc1, lo, hi);
+        s1 = warp_sum(lo + hi);
+      }
+    }
+    if (WPR > 1) {
+      if (lane == 0) {
+        red[0][warp] = s0;
+        red[1][warp] = s1;
+      }
+      __syncthreads();
+      if (t == 0) {
+        float a0 = 0.0f, a1 = 0.0f;
+        for (int w = 0; w < WPR; ++w) {
+          a0 += red[0][warp + w];
+          a1 += red[1][warp + w];
+        }
+        s0 = a0;
+        s1 = a1;
+      }
+      __syncthreads();
+    }
+    if (t == 0 && row < rows) {
+      const uint16_t gb = f32_to_bf16(G.s[0][row] * s0);
+      if (DUAL) {
+        const uint16_t ub = f32_to_bf16(G.s[1][row] * s1);
+        G.out[0][row] = SILU ? f32_to_bf16(silu_mul_f32(bf16_to_f32(gb), bf16_to_f32(ub))) : gb;
+        G.out[1][row] = ub;
+      } else {
+        G.out[0][row] = gb;
+      }
     }
   }
-  cp_async_wait<0>();
 }
 
-template <int NMAT, bool SILU>
-cudaError_t launch_t(Gemv G, bool pdl, cudaStream_t s) {
-  int parts = (G.cols + kPartMax - 1) / kPartMax;
-  G.team = 1;
-  while (G.team < parts) G.team <<= 1;
-  if (G.team > 8) return cudaErrorInvalidValue;         // cols > 32768
-  G.kpart = ((G.cols + G.team - 1) / G.team + 15) / 16 * 16;
-  const size_t xbytes = (size_t(G.cols) * 2 + 127) / 128 * 128;
-  const int stage_bytes = NMAT * kMatStage;
-  int ns = int((kSmemBudget - int64_t(xbytes) - 1024) / (int64_t(kWarps) * stage_bytes));
-  if (ns > 8) ns = 8;
-  if (ns < 2) return cudaErrorInvalidValue;
-  G.nstage = ns;
-  const size_t smem = xbytes + size_t(kWarps) * ns * stage_bytes;
-  auto fn = gemv_kernel<NMAT, SILU>;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+template <bool DUAL, bool SILU, int TPR>
+cudaError_t launch_t(const Gemv& G, bool pdl, cudaStream_t s) {
+  const size_t smem = size_t(G.cols) * 2;
+  auto fn = gemv_kernel<DUAL, SILU, TPR>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+  }
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem);
   if (e != cudaSuccess) return e;
-  const int nblocks = (G.rows + kBlockRows - 1) / kBlockRows;
-  const int nteams = kWarps / G.team;
-  const int needed = (nblocks + nteams - 1) / nteams;
-  const int grid = needed < num_sms() ? needed : num_sms();
+  if (per_sm < 1) per_sm = 1;
+  constexpr int RPB = kThreads / TPR;
+  const int needed = (G.rows + RPB - 1) / RPB;
+  const int cap = num_sms() * per_sm;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(needed < cap ? needed : cap);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -278,6 +170,15 @@ cudaError_t launch_t(Gemv G, bool pdl, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, fn, G);
+}
+
+template <bool DUAL, bool SILU>
+cudaError_t launch_d(const Gemv& G, bool pdl, cudaStream_t s) {
+  const int nchunk = G.cols / 16;
+  if (nchunk <= 32 * kU) return launch_t<DUAL, SILU, 32>(G, pdl, s);
+  if (nchunk <= 64 * kU) return launch_t<DUAL, SILU, 64>(G, pdl, s);
+  if (nchunk <= 128 * kU) return launch_t<DUAL, SILU, 128>(G, pdl, s);
+  return launch_t<DUAL, SILU, 256>(G, pdl, s);
 }
 
 }  // namespace
@@ -296,24 +197,26 @@ cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const
   G.s[1] = s1;
   G.rows = int(rows);
   G.cols = int(cols);
-  return w1 != nullptr ? launch_t<2, false>(G, pdl, s) : launch_t<1, false>(G, pdl, s);
+  return w1 != nullptr ? launch_d<true, false>(G, pdl, s) : launch_d<false, false>(G, pdl, s);
 }
 
 cudaError_t launch_decode(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
                           const float* s_gate, const uint8_t* w_up, const float* s_up,
                           const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
                           uint16_t* g, uint16_t* u, cudaStream_t s) {
-  cudaError_t e = launch_gemv(g, u, x, w_gate, s_gate, w_up, s_up, H, C, false, s);
-  if (e != cudaSuccess) return e;
   Gemv G{};
-  G.out[0] = out;
-  G.x = g;
-  G.u = u;
-  G.w[0] = w_down;
-  G.s[0] = s_down;
-  G.rows = int(C);
-  G.cols = int(H);
-  return launch_t<1, true>(G, true, s);
+  G.out[0] = g;                      // receives h = bf16(silu(g) * u)
+  G.out[1] = u;
+  G.x = x;
+  G.w[0] = w_gate;
+  G.s[0] = s_gate;
+  G.w[1] = w_up;
+  G.s[1] = s_up;
+  G.rows = int(H);
+  G.cols = int(C);
+  cudaError_t e = launch_d<true, true>(G, false, s);
+  if (e != cudaSuccess) return e;
+  return launch_gemv(out, nullptr, g, w_down, s_down, nullptr, nullptr, C, H, true, s);
 }
 
 cudaError_t decode_take_status(unsigned int* status) {
