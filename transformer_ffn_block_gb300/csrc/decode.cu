@@ -28,7 +28,8 @@ namespace qffn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kU = 8;
+constexpr int kUSingle = 8;                // 16-byte loads in flight per thread
+constexpr int kUDual = 4;                  //   (per matrix)
 
 QFFN_DEVI uint64_t e4m3x2_to_f2(uint32_t two_codes) {
   uint32_t h;
@@ -62,6 +63,7 @@ struct Gemv {
 // as the split-SiLU arm leaves h in the gate buffer.
 template <bool DUAL, bool SILU, int TPR>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
+  constexpr int kU = DUAL ? kUDual : kUSingle;
   extern __shared__ uint4 xs[];
   __shared__ float red[2][kThreads / 32];
   constexpr int RPB = kThreads / TPR;   // rows per block step
@@ -174,11 +176,9 @@ cudaError_t launch_t(const Gemv& G, bool pdl, cudaStream_t s) {
 
 template <bool DUAL, bool SILU>
 cudaError_t launch_d(const Gemv& G, bool pdl, cudaStream_t s) {
-  const int nchunk = G.cols / 16;
-  if (nchunk <= 32 * kU) return launch_t<DUAL, SILU, 32>(G, pdl, s);
-  if (nchunk <= 64 * kU) return launch_t<DUAL, SILU, 64>(G, pdl, s);
-  if (nchunk <= 128 * kU) return launch_t<DUAL, SILU, 128>(G, pdl, s);
-  return launch_t<DUAL, SILU, 256>(G, pdl, s);
+  // one warp per row at every row length: the memory system is kept busy by
+  // the number of rows in flight, and no cross-warp sums are needed
+  return launch_t<DUAL, SILU, 32>(G, pdl, s);
 }
 
 }  // namespace
