@@ -20,7 +20,9 @@
 // leaves h = bf16(silu(g) * u) in the gate buffer (the split-SiLU arm's
 // buffer use); the down GEMV on h is a programmatic dependent launch whose
 // CTAs start as the dual GEMV's CTAs retire and wait for h only right before
-// reading it.
+// reading it.  Each GEMV issues its first weight loads before that wait, and
+// the decode's dual GEMV is itself a programmatic dependent launch, so weight
+// streaming starts while the preceding kernel on the stream drains.
 #include "common.cuh"
 #include "launch.h"
 
@@ -74,6 +76,26 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = threadIdx.x / TPR, t = threadIdx.x % TPR;
 
+  // The weights do not depend on the preceding kernel: each team issues the
+  // first batch of its first row before waiting for x.
+  uint4 a[kU], b[kU];
+  bool have = false;
+  {
+    const int row = blockIdx.x * RPB + sub;
+    if (row < rows) {
+      const uint8_t* r0 = G.w[0] + size_t(row) * size_t(cols);
+      const uint8_t* r1 = DUAL ? G.w[1] + size_t(row) * size_t(cols) : nullptr;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int cc = t + TPR * u;
+        if (cc < nchunk) {
+          a[u] = ld16_ro_stream(r0 + size_t(cc) * 16);
+          if (DUAL) b[u] = ld16_ro_stream(r1 + size_t(cc) * 16);
+        }
+      }
+      have = true;
+    }
+  }
   pdl_wait();                        // x may come from the preceding kernel
   pdl_trigger();
   for (int i = threadIdx.x; i < nvec; i += kThreads) xs[i] = ld16_once(G.x + size_t(i) * 8);
@@ -86,15 +108,17 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
       const uint8_t* r0 = G.w[0] + size_t(row) * size_t(cols);
       const uint8_t* r1 = DUAL ? G.w[1] + size_t(row) * size_t(cols) : nullptr;
       for (int c = t; c < nchunk; c += TPR * kU) {
-        uint4 a[kU], b[kU];
+        if (!have) {
 #pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int cc = c + TPR * u;
-          if (cc < nchunk) {
-            a[u] = ld16_ro_stream(r0 + size_t(cc) * 16);
-            if (DUAL) b[u] = ld16_ro_stream(r1 + size_t(cc) * 16);
+          for (int u = 0; u < kU; ++u) {
+            const int cc = c + TPR * u;
+            if (cc < nchunk) {
+              a[u] = ld16_ro_stream(r0 + size_t(cc) * 16);
+              if (DUAL) b[u] = ld16_ro_stream(r1 + size_t(cc) * 16);
+            }
           }
         }
+        have = false;
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           const int cc = c + TPR * u;
@@ -214,7 +238,7 @@ cudaError_t launch_decode(uint16_t* out, const uint16_t* x, const uint8_t* w_gat
   G.s[1] = s_up;
   G.rows = int(H);
   G.cols = int(C);
-  cudaError_t e = launch_d<true, true>(G, false, s);
+  cudaError_t e = launch_d<true, true>(G, true, s);
   if (e != cudaSuccess) return e;
   return launch_gemv(out, nullptr, g, w_down, s_down, nullptr, nullptr, C, H, true, s);
 }
