@@ -9,24 +9,33 @@
 // LLamaModel::_forward_block (forward_qmm -> matmul with weight and
 // activation scales; the up projection followed by swiglu_forward).
 //
-// Design (one persistent CTA per SM, 192 threads, warp-specialised):
-//   warp 0      TMA producer: 128x128-byte A tiles and two 128x128-byte B
-//               tiles per stage, 128-byte swizzle, into a 4-stage ring.
-//   warp 1      allocates 512 TMEM columns; one thread issues
-//               tcgen05.mma.kind::f8f6f4 (M=128, N=256, K=32) and commits
-//               stage / accumulator barriers.
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (one TMEM lane
-//               quarter per warp, one output row per thread), scaling,
-//               bf16 rounding, SwiGLU, abs-max, 16-byte stores.
+// Design: SM pairs.  The grid is a set of 2-CTA clusters, one CTA per SM,
+// persistent over 256 x 256 output tiles.  Each tile is one chain of
+// tcgen05.mma.cta_group::2 (M=256, N=256, K=32) issued by the pair's leader:
+// CTA rank r stages rows [128r, 128r+128) of the tile's A slice and rows
+// [128r, 128r+128) of its B slice, so per stage an SM loads 16 KB of A and
+// 16 KB of B instead of the 16 + 32 KB a one-SM 128 x 256 tile needs, and
+// accumulates its own 128 rows x 256 columns in its own TMEM.
+//   warp 0      TMA producer (both CTAs): 128x128-byte boxes, 128-byte
+//               swizzle, into a 6-stage ring; the loads of both CTAs
+//               complete on the leader's stage barrier.
+//   warp 1      allocates 512 TMEM columns (pair-wide allocation); in the
+//               leader one thread issues the MMAs and commits stage /
+//               accumulator barriers to both CTAs at once (multicast).
+//   warps 2..5  epilogue (both CTAs): tcgen05.ld of the fp32 accumulator
+//               (one TMEM lane quarter per warp, one output row per thread),
+//               scaling, bf16 rounding, SwiGLU, abs-max, 16-byte stores; the
+//               accumulator is handed back to the leader's MMA thread by a
+//               remote mbarrier arrive.
 // Two 256-column accumulators in TMEM let the epilogue of tile i overlap the
-// MMAs of tile i+1.  For the SwiGLU form the 256 B rows of a stage are the
-// 128 gate rows followed by the 128 matching up rows, so one N=256 MMA yields
-// gate in accumulator columns [0,128) and up in [128,256).
+// MMAs of tile i+1.  In the SwiGLU form CTA 0 stages 128 gate rows and CTA 1
+// the matching 128 up rows, so the accumulator holds gate in columns
+// [0,128) and up in [128,256) for each row.
 //
 // Every mbarrier wait is bounded (about 2 s on %globaltimer); a wait that
-// runs out raises a CTA abort flag and the device status word, all roles
-// leave their loops, in-flight TMA loads and MMAs are drained (again
-// bounded), TMEM is freed and the kernel returns.
+// runs out raises the CTA's abort flag and the device status word, all roles
+// leave their loops, in-flight MMAs are drained (again bounded), both CTAs
+// meet at a final cluster barrier, TMEM is freed and the kernel returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -37,26 +46,28 @@
 namespace qffn {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;        // rows of A per CTA (256 per pair)
+constexpr int BN = 256;        // accumulator columns (N of one MMA)
 constexpr int BK = 128;        // bytes (= E4M3 elements) of K per stage: one swizzle atom row
 constexpr int UMMA_K = 32;     // K of one kind::f8f6f4 MMA
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK;
-constexpr int B_BYTES = BN * BK;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK;           // this CTA's A rows of a stage
+constexpr int B_BYTES = (BN / 2) * BK;     // this CTA's half of the B rows of a stage
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_BARS = 2 * STAGES + 5;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + NUM_BARS * 8 + 16;
-constexpr int GROUP_M = 16;    // tile raster: 16 M-blocks sweep the N-blocks together
+constexpr int GROUP_M = 8;     // tile raster: 8 pair M-blocks (2048 rows) sweep the N-blocks together
+constexpr uint16_t kBothCtas = 0x3;
+constexpr uint16_t kLeaderOnly = 0x1;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned long long kDrainLimitNs = 200000000ull;
 
 // Instruction descriptor of tcgen05.mma.kind::f8f6f4: D f32 (bits 4-5 = 1),
 // A and B E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
-// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28 (M = 256 over the CTA pair).
+constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t((2 * BM) >> 4) << 24);
 
 __device__ unsigned int g_status;
 
@@ -76,9 +87,68 @@ QFFN_DEVI bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag
   return mbar_wait_bounded(bar, parity, abort_flag, &g_status, honour_abort, limit);
 }
 
-QFFN_DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+// Same, with cluster-scope acquire: for a barrier that the peer CTA arrives on.
+QFFN_DEVI bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+QFFN_DEVI bool mbar_wait_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(&g_status, 1u);
+        return false;
+      }
+    }
+  }
+}
+
+QFFN_DEVI uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+QFFN_DEVI uint32_t cluster_id_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+QFFN_DEVI uint32_t num_clusters_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+QFFN_DEVI uint32_t map_to_rank(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+QFFN_DEVI void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+QFFN_DEVI void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// 2-D tile load whose completion is signalled on a barrier of either CTA of
+// the pair (`bar` is a shared::cluster address).
+QFFN_DEVI void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
@@ -103,16 +173,21 @@ QFFN_DEVI uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
-QFFN_DEVI void mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+// D(tmem, both CTAs) (+)= A(smem, both CTAs) . B(smem, both CTAs)^T
+QFFN_DEVI void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
       : "memory");
 }
-QFFN_DEVI void mma_commit(uint32_t bar) {
+// Arrive once on the barrier at offset `bar` of every CTA in `mask` when all
+// previously issued MMAs of this thread have completed.
+QFFN_DEVI void mma_commit_mc(uint32_t bar, uint16_t mask) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
       : "memory");
 }
 
@@ -135,6 +210,7 @@ QFFN_DEVI void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&a)[32], uint32_t
       : "memory");
 }
 
+// Pair tile -> (pair M-block of 256 rows, N-block)
 QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
   const int per_group = GROUP_M * a.tiles_n;
   const int group = tile / per_group;
@@ -158,6 +234,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
+  // Barriers (same offsets in both CTAs):
+  //   full[s]    leader: both CTAs' loads of stage s landed (1 arrival + tx)
+  //   empty[s]   each CTA: the MMAs reading stage s are done (leader's commit)
+  //   tfull[a]   each CTA: accumulator a holds a finished tile (leader's commit)
+  //   tempty[a]  leader: both CTAs' epilogues have read accumulator a (8 warps)
+  //   drain      leader: all MMAs issued have completed
   auto full_bar = [&](int s) { return bar0 + 8u * uint32_t(s); };
   auto empty_bar = [&](int s) { return bar0 + 8u * uint32_t(STAGES + s); };
   auto tfull_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + a); };
@@ -165,6 +247,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = int(cluster_id_x()), num_pairs = int(num_clusters_x());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -173,7 +257,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), 8);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -184,14 +268,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmB);
   }
   if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(tmem_slot)),
                  "r"(TMEM_COLS)
                  : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   tc_fence_before();
-  __syncthreads();
+  // both CTAs' barriers are initialised before either CTA signals the other's
+  cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -201,41 +286,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued = 0, issued_parity = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x) {
+      for (int tile = pair; ok && tile < args.num_tiles; tile += num_pairs) {
         int mb, nb;
         tile_coords(tile, args, mb, nb);
-        const int rowA = mb * BM;
-        const int rowB0 = SWIGLU ? nb * 128 : nb * BN;
-        const int rowB1 = SWIGLU ? args.H + nb * 128 : nb * BN + 128;
+        const int rowA = mb * (2 * BM) + int(rank) * BM;
+        const int rowB = SWIGLU ? (rank == 0 ? nb * 128 : args.H + nb * 128) : nb * BN + int(rank) * 128;
         for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = uint32_t(it / STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_expect_tx(full_bar(s), STAGE_BYTES);
-          const uint32_t a_dst = smem_u32(sA + s * A_BYTES);
-          const uint32_t b_dst = smem_u32(sB + s * B_BYTES);
-          tma_load_2d(a_dst, &tmA, full_bar(s), kb * BK, rowA);
-          tma_load_2d(b_dst, &tmB, full_bar(s), kb * BK, rowB0);
-          tma_load_2d(b_dst + 128 * BK, &tmB, full_bar(s), kb * BK, rowB1);
+          if (rank == 0) mbar_expect_tx(full_bar(s), 2 * STAGE_BYTES);
+          const uint32_t fb = map_to_rank(full_bar(s), 0);
+          tma_load_2d_pair(smem_u32(sA + s * A_BYTES), &tmA, fb, kb * BK, rowA);
+          tma_load_2d_pair(smem_u32(sB + s * B_BYTES), &tmB, fb, kb * BK, rowB);
           issued |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
         }
       }
-      // drain: every load this thread issued has landed before smem is released
-      for (int s = 0; s < STAGES; ++s)
-        if (issued & (1u << s))
-          mbar_wait(full_bar(s), (issued_parity >> s) & 1u, abort_flag, false, kDrainLimitNs);
+      // drain (leader): every phase it armed has completed, so both CTAs'
+      // loads into those stages have landed before shared memory is released
+      if (rank == 0)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s))
+            mbar_wait(full_bar(s), (issued_parity >> s) & 1u, abort_flag, false, kDrainLimitNs);
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && rank == 0) {
+      // ------------------------------------------------------------ MMA issuer (leader)
       int it = 0, local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < args.num_tiles; tile += gridDim.x, ++local) {
+      for (int tile = pair; ok && tile < args.num_tiles; tile += num_pairs, ++local) {
         const int acc = local & 1;
         const uint32_t aph = uint32_t(local >> 1) & 1u;
-        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) break;
+        if (!mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
@@ -247,33 +331,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b0 = smem_u32(sB + s * B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk)
-            mma_f8(d_tmem, sdesc_sw128(a0 + kk * UMMA_K), sdesc_sw128(b0 + kk * UMMA_K),
-                   uint32_t(kb | kk));
-          mma_commit(empty_bar(s));
+            mma_f8_pair(d_tmem, sdesc_sw128(a0 + kk * UMMA_K), sdesc_sw128(b0 + kk * UMMA_K),
+                        uint32_t(kb | kk));
+          mma_commit_mc(empty_bar(s), kBothCtas);
         }
         if (!ok) break;
-        mma_commit(tfull_bar(acc));
+        mma_commit_mc(tfull_bar(acc), kBothCtas);
       }
       // drain: all MMAs issued by this thread have completed
-      mma_commit(drain_bar);
+      mma_commit_mc(drain_bar, kLeaderOnly);
       mbar_wait(drain_bar, 0, abort_flag, false, kDrainLimitNs);
     }
     __syncwarp();
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;                  // TMEM lane quarter of this warp
-    const int row_in_tile = q * 32 + lane;
+    const int row_in_tile = int(rank) * BM + q * 32 + lane;
     const float scale = args.a_scale[0] * args.w_scale[0];
     float amax = 0.0f;
     int local = 0;
-    for (int tile = blockIdx.x; tile < args.num_tiles; tile += gridDim.x, ++local) {
+    for (int tile = pair; tile < args.num_tiles; tile += num_pairs, ++local) {
       const int acc = local & 1;
       const uint32_t aph = uint32_t(local >> 1) & 1u;
       if (!mbar_wait(tfull_bar(acc), aph, abort_flag)) break;
       tc_fence_after();
       int mb, nb;
       tile_coords(tile, args, mb, nb);
-      const int row = mb * BM + row_in_tile;
+      const int row = mb * (2 * BM) + row_in_tile;
       const bool row_ok = row < args.M;
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
       if (!SWIGLU) {
@@ -308,7 +392,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float u0 = round_bf16(__uint_as_float(u[2 * j]) * scale);
             const float u1 = round_bf16(__uint_as_float(u[2 * j + 1]) * scale);
             p[j] = pack_bf16x2(silu_mul_f32(g0, u0), silu_mul_f32(g1, u1));
-            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
+            if (row_ok) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
           }
           if (row_ok) {
 #pragma unroll
@@ -319,7 +403,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (lane == 0) mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
     }
     if (SWIGLU) {
       amax = warp_max(amax);
@@ -327,11 +411,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
 
+  // Both CTAs finish together: the leader's MMAs write the peer's TMEM and
+  // both CTAs signal barriers of the other, so neither frees TMEM or exits
+  // while the other may still touch it.
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(TMEM_COLS)
                  : "memory");
   }
@@ -364,21 +452,60 @@ bool make_map(CUtensorMap* map, const uint8_t* ptr, int64_t rows, int64_t k) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Number of 2-CTA clusters of this kernel that fit on the device at once
+// (cached per device and form).
 template <bool SWIGLU>
-cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s) {
-  static int attr_done[64] = {0};
+cudaError_t max_pairs(int* pairs) {
+  static int cached[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-    e = cudaFuncSetAttribute(gemm_fp8_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = 1;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) {
+    *pairs = cached[dev];
+    return cudaSuccess;
   }
-  const int grid = a.num_tiles < num_sms() ? a.num_tiles : num_sms();
-  gemm_fp8_kernel<SWIGLU><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(ma, mb, a);
-  return cudaGetLastError();
+  e = cudaFuncSetAttribute(gemm_fp8_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (num_sms() / 2));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<SWIGLU>, &cfg);
+  if (e != cudaSuccess) return e;
+  if (n < 1) return cudaErrorInvalidConfiguration;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  *pairs = n;
+  return cudaSuccess;
+}
+
+template <bool SWIGLU>
+cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s) {
+  int pairs = 0;
+  cudaError_t e = max_pairs<SWIGLU>(&pairs);
+  if (e != cudaSuccess) return e;
+  if (a.num_tiles < pairs) pairs = a.num_tiles;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<SWIGLU>, ma, mb, a);
 }
 
 }  // namespace
@@ -398,7 +525,7 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.N = int(N);
   a.K = int(K);
   a.H = 0;
-  a.tiles_m = int((M + BM - 1) / BM);
+  a.tiles_m = int((M + 2 * BM - 1) / (2 * BM));
   a.tiles_n = int((N + BN - 1) / BN);
   a.num_tiles = a.tiles_m * a.tiles_n;
   a.num_kb = int((K + BK - 1) / BK);
@@ -421,7 +548,7 @@ cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, co
   a.N = int(H);
   a.K = int(K);
   a.H = int(H);
-  a.tiles_m = int((M + BM - 1) / BM);
+  a.tiles_m = int((M + 2 * BM - 1) / (2 * BM));
   a.tiles_n = int(H / 128);
   a.num_tiles = a.tiles_m * a.tiles_n;
   a.num_kb = int((K + BK - 1) / BK);
