@@ -38,6 +38,12 @@ METRIC = "FP8 SwiGLU-FFN fwd TFLOP/s (8B shape, 16k tok)"
 DECODE_METRIC = "M=1 decode FFN HBM GB/s"
 L2_BYTES = 129 * 1024 * 1024
 FP8_PER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor rate ratio
+# DRAM bytes (read + write) per launch of the dominant kernels, from one ncu
+# capture of this benchmark's full-size workload (dram__bytes_read.sum +
+# dram__bytes_write.sum, summarised in profiles/launches_llama3-8b_ffn.md).
+# Set to None whenever the kernel changes until it is captured again.
+TRAFFIC_GATE_UP_BYTES = (1009.9 + 447.5) * 1e6
+TRAFFIC_DUAL_GEMV_BYTES = (117.6 + 0.1) * 1e6
 
 
 def load_peaks():
@@ -315,7 +321,8 @@ def bench_prefill(q, torch, device, steps, warmup, dist, peaks):
                      "down_gemm": stage_ms[4], "staged_total": staged_total},
         "roofline": {"bound": "tensor", "kernel": "gemm_fp8_kernel<swiglu> (gate|up GEMM + SwiGLU)",
                      "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": achieved / fp8_peak, "traffic": None,
+                     "frac": achieved / fp8_peak, "traffic": TRAFFIC_GATE_UP_BYTES,
+                     "traffic_unit": "bytes per launch",
                      "peak_note": f"{peaks['source']} bf16 burst x {FP8_PER_BF16:g} (nominal FP8/BF16 ratio)"},
         "clocks": clk.summary(),
         "launches_per_step": 5,
@@ -409,7 +416,8 @@ def bench_decode(q, torch, device, iters, dist, peaks):
         "ungraphed_us_per_call": ungraphed_us, "weight_copies_rotated": copies,
         "roofline": {"bound": "hbm", "kernel": "gemv_kernel<dual> (gate+up GEMV)",
                      "achieved": dual_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": dual_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": dual_gbs / peaks["hbm_gbs"], "traffic": TRAFFIC_DUAL_GEMV_BYTES,
+                     "traffic_unit": "bytes per launch",
                      "peak_note": f"{peaks['source']} HBM copy bandwidth"},
         "stage_us": {"gemv_dual": dual_us, "gemv_down": down_us},
         "frac_of_peak": gbs / peaks["hbm_gbs"],
