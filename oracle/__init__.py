@@ -13,8 +13,9 @@ It is a plain, slow, float64 restatement of what the pages compute:
   definitions (round to nearest even; E4M3 saturating at 448).
 * ``ffn``     -- the prefill chain (fused residual + RMSNorm + abs-max,
   per-tensor quantisation, scaled FP8 GEMMs, SwiGLU with abs-max and
-  requantisation) and the single-token decode FFN (dual row-scaled GEMV,
-  silu_mul, down GEMV).
+  requantisation), its recompute form with the activation abs-maxes given
+  (``swiglu_forward_quant``, ``ffn_forward_recompute``), and the single-token
+  decode FFN (dual row-scaled GEMV, silu_mul, down GEMV).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against hand-worked
 values (``tests/golden/``), closed forms, invariants, library cross-checks
@@ -22,15 +23,15 @@ and brute-force exact arithmetic on tiny inputs (``tests/brute.py``).
 """
 from .codecs import (E4M3_MAX, bf16_to_f32, bf16_to_f64, e4m3_decode, e4m3_encode,
                      e4m3_to_scaled_int, f32_to_bf16, f64_to_bf16)
-from .ffn import (absmax, decode_forward, ffn_forward, fp8_gemm_scaled, gemv_dual,
-                  gemv_row_scaled, quantize_rows, quantize_tensor, quantize_with_abs_max,
-                  residual_rmsnorm_absmax, rmsnorm_f64, silu_f64, silu_mul, swiglu,
-                  swiglu_quant)
+from .ffn import (absmax, decode_forward, ffn_forward, ffn_forward_recompute, fp8_gemm_scaled,
+                  gemv_dual, gemv_row_scaled, quantize_rows, quantize_tensor,
+                  quantize_with_abs_max, residual_rmsnorm_absmax, rmsnorm_f64, silu_f64,
+                  silu_mul, swiglu, swiglu_forward_quant, swiglu_quant)
 
 __all__ = [
     "E4M3_MAX", "bf16_to_f32", "bf16_to_f64", "e4m3_decode", "e4m3_encode",
     "e4m3_to_scaled_int", "f32_to_bf16", "f64_to_bf16", "absmax", "decode_forward",
-    "ffn_forward", "fp8_gemm_scaled", "gemv_dual", "gemv_row_scaled", "quantize_rows",
+    "ffn_forward", "ffn_forward_recompute", "fp8_gemm_scaled", "gemv_dual", "gemv_row_scaled", "quantize_rows",
     "quantize_tensor", "quantize_with_abs_max", "residual_rmsnorm_absmax", "rmsnorm_f64",
-    "silu_f64", "silu_mul", "swiglu", "swiglu_quant",
+    "silu_f64", "silu_mul", "swiglu", "swiglu_forward_quant", "swiglu_quant",
 ]

@@ -204,6 +204,20 @@ def swiglu_quant(gu_bits, H: int):
     return h, hq, np.array([amax, scale], dtype=np.float32)
 
 
+def swiglu_forward_quant(gu_bits, H: int, amax):
+    """Step A4 in the recompute form: SwiGLU quantised with an abs-max given, not recorded.
+
+    [llmq-model] ``_recompute_block``: ``swiglu_forward_quant(SwiGLu.Quant,
+    SwiGLu.Quant.scale(), MlpUp, SwiGLu.Quant.abs_max(), B, T, D)`` reads the
+    abs-max the forward left in the stats slot and writes the FP8 copy and
+    its scale.  h is the bf16 SwiGLU value of ``swiglu`` (R9, R10); it is
+    quantised by A2's rule with the given abs-max (R2, R6, R7), and values
+    beyond that abs-max saturate at +-448 (R8).  Returns ``(hq codes, scale)``.
+    """
+    h, _ = swiglu(gu_bits, H)
+    return quantize_with_abs_max(h, amax)
+
+
 # ------------------------------------------------------------------ A1..A5
 def ffn_forward(res_bits, x_bits, gain_bits, eps, w1_codes, w1_scale, w2_codes, w2_scale, H: int):
     """The whole prefill FFN chain A1..A5 [llmq-model ``_forward_block``, FFN half].
@@ -220,6 +234,36 @@ def ffn_forward(res_bits, x_bits, gain_bits, eps, w1_codes, w1_scale, w2_codes, 
     return {
         "r": r, "y": y, "rstd": rstd, "stats_y": np.array([amax_y, sy], dtype=np.float32),
         "yq": yq, "gu": gu, "h": h, "stats_h": stats_h, "hq": hq, "out": out,
+    }
+
+
+def ffn_forward_recompute(res_bits, x_bits, gain_bits, eps, w1_codes, w1_scale, w2_codes,
+                          w2_scale, H: int, amax_y, amax_h):
+    """The prefill chain with both activation abs-maxes given instead of recorded.
+
+    [llmq-model] ``_recompute_block``, FFN half:
+    - the norm is re-run without recording an abs-max
+      (``fused_residual_rmsnorm_forward(..., nullptr, eps, ...)``);
+    - the up projection's ``forward_qmm`` quantises LN2 with the abs-max its
+      stats slot still holds;
+    - ``swiglu_forward_quant`` quantises h with the recorded SwiGLU abs-max.
+
+    The recompute block stops at the quantised h.  This chain then applies the
+    down projection exactly as the forward does (``forward_qmm`` on the down
+    weight with the SwiGLU scale), so it yields the block output.  Given the
+    abs-maxes that ``ffn_forward`` recorded, every result equals that forward's.
+    Returns r, y, rstd, stats_y, yq, gu, hq, stats_h, out.
+    """
+    r, y, rstd, _ = residual_rmsnorm_absmax(res_bits, x_bits, gain_bits, eps)
+    amax_y, amax_h = np.float32(amax_y), np.float32(amax_h)
+    yq, sy = quantize_with_abs_max(y, amax_y)
+    gu = fp8_gemm_scaled(yq, sy, w1_codes, w1_scale)
+    hq, sh = swiglu_forward_quant(gu, H, amax_h)
+    out = fp8_gemm_scaled(hq, sh, w2_codes, w2_scale)
+    return {
+        "r": r, "y": y, "rstd": rstd, "stats_y": np.array([amax_y, sy], dtype=np.float32),
+        "yq": yq, "gu": gu, "hq": hq, "stats_h": np.array([amax_h, sh], dtype=np.float32),
+        "out": out,
     }
 
 

@@ -304,3 +304,79 @@ def test_planted_gate_up_swap_is_caught(monkeypatch):
         for i in range(3):
             for j in range(H):
                 assert int(h[i, j]) == brute.silu_times(gu[i, j], gu[i, H + j])
+
+
+# ------------------------------------------------------------------ recompute form (given abs-max)
+def test_swiglu_forward_quant_given_absmax_matches_brute_force():
+    """A4 with the abs-max given: the codes of the exact-arithmetic quantiser, also
+    when the given abs-max is below the true one (every element beyond it saturates)."""
+    H = 16
+    gu = _mixed_bf16((4, 2 * H), 91)
+    h, amax = oracle.swiglu(gu, H)
+    # Fractions have no signed zero: an input of -0.0 (silu underflow) keeps its
+    # sign in the E4M3 encoding (code 0x80) where the brute force says 0.
+    negzero = [int(b) == 0x8000 for b in h.ravel()]
+    for given in (amax, np.float32(amax * np.float32(0.25)), np.float32(amax * np.float32(3.0))):
+        hq, scale = oracle.swiglu_forward_quant(gu, H, given)
+        bq, bs = brute.quantize(list(h.ravel()), float(given))
+        bq = [0x80 if nz else c for c, nz in zip(bq, negzero)]
+        assert list(hq.ravel()) == bq
+        assert Fraction(float(scale)) == bs
+    # below the true abs-max: saturated codes are exactly the elements whose
+    # fp32-scaled value is at or above 432 (the tie between 416 and 448 rounds to 448)
+    given = np.float32(amax * np.float32(0.25))
+    hq, _ = oracle.swiglu_forward_quant(gu, H, given)
+    inv = Fraction(float(np.float32(448) / given))
+    big = [abs(brute.f32(brute.bf16_value(int(b)) * inv)) >= 432 for b in h.ravel()]
+    sat = [int(c) & 0x7F == 0x7E for c in hq.ravel()]
+    assert any(big) and big == sat
+
+
+def test_swiglu_forward_quant_zero_absmax():
+    gu = _mixed_bf16((2, 16), 92)
+    hq, scale = oracle.swiglu_forward_quant(gu, 8, np.float32(0))
+    assert scale == np.float32(1.0) and not hq.any()
+
+
+def test_recompute_with_recorded_absmax_equals_forward():
+    """Re-running the chain with the abs-maxes a forward recorded reproduces it."""
+    N, C, H = 24, 64, 128
+    res, x = random_bf16((N, C), 93), random_bf16((N, C), 94)
+    gain = _bf(1 + 0.1 * np.random.default_rng(95).standard_normal(C))
+    w1q, w1s = oracle.quantize_tensor(random_bf16((2 * H, C), 96, std=0.02))
+    w2q, w2s = oracle.quantize_tensor(random_bf16((C, H), 97, std=0.02))
+    eps = np.float32(1e-5)
+    f = oracle.ffn_forward(res, x, gain, eps, w1q, w1s, w2q, w2s, H)
+    r = oracle.ffn_forward_recompute(res, x, gain, eps, w1q, w1s, w2q, w2s, H,
+                                     f["stats_y"][0], f["stats_h"][0])
+    for k in ("r", "y", "rstd", "stats_y", "yq", "gu", "hq", "stats_h", "out"):
+        np.testing.assert_array_equal(r[k], f[k], err_msg=k)
+
+
+def test_recompute_tiny_brute_force_chain():
+    """Recompute chain at N=2, C=8, H=4 with abs-maxes unrelated to the data
+    (one above, one below the recorded values) against the brute-force steps."""
+    N, C, H = 2, 8, 4
+    res, x = _mixed_bf16((N, C), 101), _mixed_bf16((N, C), 102)
+    gain = _bf(1 + 0.1 * np.random.default_rng(103).standard_normal(C))
+    w1q, w1s = oracle.quantize_tensor(random_bf16((2 * H, C), 104, std=0.02))
+    w2q, w2s = oracle.quantize_tensor(random_bf16((C, H), 105, std=0.02))
+    eps = np.float32(1e-5)
+    f = oracle.ffn_forward(res, x, gain, eps, w1q, w1s, w2q, w2s, H)
+    ay = np.float32(f["stats_y"][0] * np.float32(1.5))
+    ah = np.float32(f["stats_h"][0] * np.float32(0.5))
+    o = oracle.ffn_forward_recompute(res, x, gain, eps, w1q, w1s, w2q, w2s, H, ay, ah)
+    ys = []
+    for i in range(N):
+        _, by, _ = brute.rmsnorm_row(res[i], x[i], gain, eps)
+        ys.extend(by)
+    yq, sy = brute.quantize(ys, float(ay))
+    assert o["yq"].tolist() == [yq[i * C:(i + 1) * C] for i in range(N)]
+    assert Fraction(float(o["stats_y"][1])) == sy
+    gu = brute.gemm(o["yq"].tolist(), float(sy), w1q.tolist(), w1s)
+    assert o["gu"].tolist() == gu
+    h = [brute.silu_times(gu[i][j], gu[i][H + j]) for i in range(N) for j in range(H)]
+    hq, sh = brute.quantize(h, float(ah))
+    assert o["hq"].tolist() == [hq[i * H:(i + 1) * H] for i in range(N)]
+    assert Fraction(float(o["stats_h"][1])) == sh
+    assert o["out"].tolist() == brute.gemm(o["hq"].tolist(), float(sh), w2q.tolist(), w2s)
