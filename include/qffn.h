@@ -138,6 +138,32 @@ qffn_status qffn_gate_up_swiglu(uint16_t* h, float* stats_h, const uint8_t* yq,
 qffn_status qffn_swiglu_quant(uint16_t* h, uint8_t* hq, float* stats, const uint16_t* gate_up,
                               int64_t N, int64_t H, qffn_stream_t stream);
 
+/* ---- Step A4, recompute form: SwiGLU quantised with a given abs-max -------
+ * [llmq-model] _recompute_block: swiglu_forward_quant(SwiGLu.Quant, scale,
+ * MlpUp, SwiGLu.Quant.abs_max(), B, T, D) -- the abs-max the forward
+ * recorded is read, not recomputed.  gate_up is [N, 2H] bf16 (gate = cols
+ * [0,H)).  Reads stats[0] (abs_max, >= 0), writes stats[1] = scale and
+ *   hq[N,H] = e4m3(bf16(silu(g) * u) * 448 / abs_max)
+ * Values beyond the given abs-max saturate at +-448.  With the abs-max that
+ * qffn_swiglu_quant recorded, hq is bit-identical to that call's hq.
+ * N >= 0, H % 8 == 0. */
+qffn_status qffn_swiglu_forward_quant(uint8_t* hq, float* stats, const uint16_t* gate_up,
+                                      int64_t N, int64_t H, qffn_stream_t stream);
+
+/* ---- Steps A3 + A4 fused, recompute form: E4M3 h straight from the GEMM ---
+ * [llmq-model] _recompute_block: forward_qmm on MLP_Up_w followed by
+ * swiglu_forward_quant with the recorded abs-max.  The epilogue of the
+ * gate|up GEMM forms h exactly as qffn_gate_up_swiglu does and quantises it
+ * with the abs-max read from stats_h[0]:
+ *   hq[N,H] = e4m3(h * 448 / stats_h[0]),  stats_h[1] = scale
+ * Neither the [N, 2H] up-projection output nor bf16 h is written.  Given
+ * the abs-max qffn_gate_up_swiglu recorded, hq equals qffn_quantize of that
+ * call's h bit for bit.  Shape rules of qffn_gate_up_swiglu. */
+qffn_status qffn_gate_up_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* yq,
+                                      const float* y_scale, const uint8_t* w1,
+                                      const float* w1_scale, int64_t N, int64_t C, int64_t H,
+                                      qffn_stream_t stream);
+
 /* ---- Whole prefill FFN: A1 -> A2 -> A3+A4 -> A2 -> A5 ---------------------
  * [llmq-model] _forward_block, FFN half, for B*T tokens:
  *   r = bf16(res_in + x); y = rmsnorm(r) * gain; yq = quant(y);
@@ -160,6 +186,27 @@ qffn_status qffn_forward(uint16_t* res_out, uint16_t* out, float* rstd, float* s
                          const float* w1_scale, const uint8_t* w2, const float* w2_scale,
                          int64_t B, int64_t T, int64_t C, int64_t H, void* workspace,
                          size_t workspace_bytes, qffn_stream_t stream);
+
+/* ---- Whole prefill FFN with the activation abs-maxes given ---------------
+ * [llmq-model] _recompute_block, FFN half:
+ *   - the norm re-runs without recording an abs-max;
+ *   - LN2 is quantised with the abs-max its stats slot holds;
+ *   - swiglu_forward_quant uses the recorded SwiGLU abs-max.
+ * The down projection then runs as in the forward, so the call yields the
+ * block output.  Arguments, workspace and shape rules are those of
+ * qffn_forward, except that stats_y[0] and stats_h[0] are inputs (abs-maxes,
+ * >= 0) and only stats_y[1] and stats_h[1] (the scales) are written.  Four
+ * launches: A1 (no abs-max), A2, the gate|up GEMM with the E4M3 SwiGLU
+ * epilogue (qffn_gate_up_swiglu_quant), A5.  The h slot of the workspace is
+ * not written.  Given the stats a qffn_forward call left, every output (res_out,
+ * out, rstd, and yq and hq in the workspace) equals that call's bit for bit.
+ * Elements beyond a given abs-max saturate at +-448. */
+qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd, float* stats_y,
+                                  float* stats_h, const uint16_t* res_in, const uint16_t* x,
+                                  const uint16_t* gain, float eps, const uint8_t* w1,
+                                  const float* w1_scale, const uint8_t* w2, const float* w2_scale,
+                                  int64_t B, int64_t T, int64_t C, int64_t H, void* workspace,
+                                  size_t workspace_bytes, qffn_stream_t stream);
 
 /* ---- Step A6: dual row-scaled FP8 GEMV ------------------------------------
  * [metrale] w8a16_gemv_dual: one pass over x for two weight matrices.

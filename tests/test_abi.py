@@ -130,3 +130,26 @@ def test_python_binding_raises(lib):
     with pytest.raises(lib.QffnError) as e:
         lib.qffn_gemv(A, A, A, A, 10, 24, stream=0)
     assert e.value.status == 2
+
+
+def test_recompute_form_checks(lib):
+    f = lambda *a: _call(lib, "qffn_swiglu_forward_quant", *a)
+    assert f(A, NULL, A, 4, 64, None) == 1
+    assert f(A, A, A, 4, 12, None) == 2               # H % 8
+    assert f(MIS, A, A, 4, 64, None) == 3
+    g = lambda *a: _call(lib, "qffn_gate_up_swiglu_quant", *a)
+    assert g(A, A, A, A, A, NULL, 4, 256, 256, None) == 1
+    assert g(A, A, A, A, A, A, 4, 256, 200, None) == 2  # H % 128
+    assert g(A, A, A, A, A, A, 4, 20, 256, None) == 2   # C % 16
+    assert g(A, A, MIS, A, A, A, 4, 256, 256, None) == 3
+    h = lambda *a: _call(lib, "qffn_forward_recompute", *a)
+    ws = lib.qffn_forward_workspace_size(2, 32, 256, 768)
+    args = [A, A, A, A, A, A, A, A, 1e-5, A, A, A, A, 2, 32, 256, 768, A, ws, None]
+    bad = list(args); bad[4] = NULL                            # stats_h is required
+    assert h(*bad) == 1
+    bad = list(args); bad[18] = ws - 1
+    assert h(*bad) == 1
+    bad = list(args); bad[16] = 200                            # H % 128
+    assert h(*bad) == 2
+    bad = list(args); bad[17] = A + 16
+    assert h(*bad) == 3

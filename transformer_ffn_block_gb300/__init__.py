@@ -20,7 +20,9 @@ __all__ = [
     "qffn_status_string", "qffn_abi_version", "qffn_check_status",
     "qffn_rmsnorm_absmax", "qffn_absmax", "qffn_quantize", "qffn_quantize_rows",
     "qffn_fp8_gemm_scaled", "qffn_gate_up_swiglu", "qffn_swiglu_quant",
+    "qffn_swiglu_forward_quant", "qffn_gate_up_swiglu_quant",
     "qffn_forward_workspace_size", "qffn_forward_workspace_offsets", "qffn_forward",
+    "qffn_forward_recompute",
     "qffn_gemv_dual", "qffn_gemv", "qffn_silu_mul", "qffn_decode_workspace_size",
     "qffn_decode_forward", "qffn_decode_forward_noalloc",
 ]
@@ -52,10 +54,14 @@ _SIGS = {
     "qffn_fp8_gemm_scaled": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
     "qffn_gate_up_swiglu": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
     "qffn_swiglu_quant": ([_P, _P, _P, _P, _I64, _I64, _P], _S),
+    "qffn_swiglu_forward_quant": ([_P, _P, _P, _I64, _I64, _P], _S),
+    "qffn_gate_up_swiglu_quant": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
     "qffn_forward_workspace_size": ([_I64, _I64, _I64, _I64], _SZ),
     "qffn_forward_workspace_offsets": ([_I64, _I64, _I64, _I64, ctypes.POINTER(_SZ)], _S),
     "qffn_forward": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P,
                       _I64, _I64, _I64, _I64, _P, _SZ, _P], _S),
+    "qffn_forward_recompute": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P,
+                                _I64, _I64, _I64, _I64, _P, _SZ, _P], _S),
     "qffn_gemv_dual": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], _S),
     "qffn_gemv": ([_P, _P, _P, _P, _I64, _I64, _P], _S),
     "qffn_silu_mul": ([_P, _P, _I64, _P], _S),
@@ -146,6 +152,17 @@ def qffn_swiglu_quant(h, hq, stats, gate_up, N, H, stream=None):
         _ptr(h), _ptr(hq), _ptr(stats), _ptr(gate_up), int(N), int(H), _stream(stream)))
 
 
+def qffn_swiglu_forward_quant(hq, stats, gate_up, N, H, stream=None):
+    _check("qffn_swiglu_forward_quant", lib.qffn_swiglu_forward_quant(
+        _ptr(hq), _ptr(stats), _ptr(gate_up), int(N), int(H), _stream(stream)))
+
+
+def qffn_gate_up_swiglu_quant(hq, stats_h, yq, y_scale, w1, w1_scale, N, C, H, stream=None):
+    _check("qffn_gate_up_swiglu_quant", lib.qffn_gate_up_swiglu_quant(
+        _ptr(hq), _ptr(stats_h), _ptr(yq), _ptr(y_scale), _ptr(w1), _ptr(w1_scale),
+        int(N), int(C), int(H), _stream(stream)))
+
+
 def qffn_forward_workspace_size(B, T, C, H) -> int:
     return int(lib.qffn_forward_workspace_size(int(B), int(T), int(C), int(H)))
 
@@ -162,6 +179,17 @@ def qffn_forward(res_out, out, rstd, stats_y, stats_h, res_in, x, gain, eps, w1,
     if workspace_bytes is None:
         workspace_bytes = workspace.numel() * workspace.element_size()
     _check("qffn_forward", lib.qffn_forward(
+        _ptr(res_out), _ptr(out), _ptr(rstd), _ptr(stats_y), _ptr(stats_h), _ptr(res_in),
+        _ptr(x), _ptr(gain), float(eps), _ptr(w1), _ptr(w1_scale), _ptr(w2), _ptr(w2_scale),
+        int(B), int(T), int(C), int(H), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def qffn_forward_recompute(res_out, out, rstd, stats_y, stats_h, res_in, x, gain, eps, w1,
+                           w1_scale, w2, w2_scale, B, T, C, H, workspace, workspace_bytes=None,
+                           stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("qffn_forward_recompute", lib.qffn_forward_recompute(
         _ptr(res_out), _ptr(out), _ptr(rstd), _ptr(stats_y), _ptr(stats_h), _ptr(res_in),
         _ptr(x), _ptr(gain), float(eps), _ptr(w1), _ptr(w1_scale), _ptr(w2), _ptr(w2_scale),
         int(B), int(T), int(C), int(H), _ptr(workspace), int(workspace_bytes), _stream(stream)))

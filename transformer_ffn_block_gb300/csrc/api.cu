@@ -163,6 +163,31 @@ qffn_status qffn_swiglu_quant(uint16_t* h, uint8_t* hq, float* stats, const uint
   return from_cuda(qffn::launch_swiglu_requant(hq, stats, gate_up, N, H, stream));
 }
 
+qffn_status qffn_swiglu_forward_quant(uint8_t* hq, float* stats, const uint16_t* gate_up,
+                                      int64_t N, int64_t H, qffn_stream_t stream) {
+  QFFN_PTR(hq); QFFN_PTR(stats); QFFN_PTR(gate_up);
+  QFFN_REQUIRE(N >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(H % 8 == 0 && H >= 8 && H <= kMaxDim && N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(hq); QFFN_ALIGNED4(stats); QFFN_ALIGNED(gate_up);
+  return from_cuda(qffn::launch_swiglu_requant(hq, stats, gate_up, N, H, stream));
+}
+
+qffn_status qffn_gate_up_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* yq,
+                                      const float* y_scale, const uint8_t* w1,
+                                      const float* w1_scale, int64_t N, int64_t C, int64_t H,
+                                      qffn_stream_t stream) {
+  QFFN_PTR(hq); QFFN_PTR(stats_h); QFFN_PTR(yq); QFFN_PTR(y_scale); QFFN_PTR(w1); QFFN_PTR(w1_scale);
+  QFFN_REQUIRE(N >= 0 && C >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(C % 16 == 0 && C >= 16 && C <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(H % 128 == 0 && H >= 128 && H <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE((N + 127) / 128 * (H / 128) < (int64_t(1) << 31), QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(hq); QFFN_ALIGNED4(stats_h); QFFN_ALIGNED(yq); QFFN_ALIGNED(w1);
+  QFFN_ALIGNED4(y_scale); QFFN_ALIGNED4(w1_scale);
+  return from_cuda(
+      qffn::launch_gemm_swiglu_quant(hq, stats_h, yq, y_scale, w1, w1_scale, N, H, C, stream));
+}
+
 size_t qffn_forward_workspace_size(int64_t B, int64_t T, int64_t C, int64_t H) {
   if (check_forward_shape(B, T, C, H) != QFFN_OK) return 0;
   size_t off[5];
@@ -218,6 +243,44 @@ qffn_status qffn_forward(uint16_t* res_out, uint16_t* out, float* rstd, float* s
   QFFN_CUDA(qffn::launch_gemm_swiglu(h, stats_h, yq, stats_y + 1, w1, w1_scale, N, H, C, stream));
   // A4 requantisation: hq, stats_h[1]
   QFFN_CUDA(qffn::launch_quantize(hq, stats_h, h, N * H, stream));
+  // A5: out
+  return from_cuda(qffn::launch_gemm_bf16(out, hq, stats_h + 1, w2, w2_scale, N, C, H, stream));
+}
+
+qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd, float* stats_y,
+                                  float* stats_h, const uint16_t* res_in, const uint16_t* x,
+                                  const uint16_t* gain, float eps, const uint8_t* w1,
+                                  const float* w1_scale, const uint8_t* w2, const float* w2_scale,
+                                  int64_t B, int64_t T, int64_t C, int64_t H, void* workspace,
+                                  size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_PTR(out); QFFN_PTR(rstd); QFFN_PTR(stats_y); QFFN_PTR(stats_h); QFFN_PTR(x);
+  QFFN_PTR(gain); QFFN_PTR(w1); QFFN_PTR(w1_scale); QFFN_PTR(w2); QFFN_PTR(w2_scale);
+  QFFN_PTR(workspace);
+  if (res_in != nullptr) QFFN_PTR(res_out);
+  QFFN_REQUIRE(isfinite(eps) && eps >= 0.0f, QFFN_ERR_INVALID_ARG);
+  const qffn_status st = check_forward_shape(B, T, C, H);
+  if (st != QFFN_OK) return st;
+  const int64_t N = B * T;
+  size_t off[5];
+  forward_offsets(N, C, H, off);
+  QFFN_REQUIRE(workspace_bytes >= off[4], QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(aligned256(workspace), QFFN_ERR_MISALIGNED);
+  QFFN_ALIGNED(out); QFFN_ALIGNED4(rstd); QFFN_ALIGNED4(stats_y); QFFN_ALIGNED4(stats_h);
+  QFFN_ALIGNED(x); QFFN_ALIGNED(gain); QFFN_ALIGNED(w1); QFFN_ALIGNED(w2);
+  QFFN_ALIGNED4(w1_scale); QFFN_ALIGNED4(w2_scale);
+  if (res_in != nullptr) { QFFN_ALIGNED(res_in); QFFN_ALIGNED(res_out); }
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* y = reinterpret_cast<uint16_t*>(ws + off[0]);
+  uint8_t* yq = ws + off[1];
+  uint8_t* hq = ws + off[3];
+
+  // A1 without recording an abs-max: r, y, rstd
+  QFFN_CUDA(qffn::launch_rmsnorm(res_out, y, rstd, nullptr, res_in, x, gain, eps, N, int(C), stream));
+  // A2 with the given abs-max of y: yq, stats_y[1]
+  QFFN_CUDA(qffn::launch_quantize(yq, stats_y, y, N * C, stream));
+  // A3 + A4 with the given abs-max of h: hq, stats_h[1] (bf16 h is never written)
+  QFFN_CUDA(qffn::launch_gemm_swiglu_quant(hq, stats_h, yq, stats_y + 1, w1, w1_scale, N, H, C, stream));
   // A5: out
   return from_cuda(qffn::launch_gemm_bf16(out, hq, stats_h + 1, w2, w2_scale, N, C, H, stream));
 }

@@ -4,10 +4,14 @@
 //   gemm_swiglu : h[M,H]    = bf16(silu(g)*u), g / u the bf16-rounded gate and
 //                 up products of W1 = [2H, K] (gate rows [0,H), up rows
 //                 [H,2H)); the tensor abs-max of h is recorded on the way.
+//   gemm_swiglu_quant : hq[M,H] = e4m3(h * 448 / amax_h) with amax_h given
+//                 (read from stats_h[0], not recorded); stats_h[1] = scale.
 //
 // These are the two matmuls of the FFN half of llmq "llama_model.cpp",
 // LLamaModel::_forward_block (forward_qmm -> matmul with weight and
-// activation scales; the up projection followed by swiglu_forward).
+// activation scales; the up projection followed by swiglu_forward), and the
+// up projection of _recompute_block followed by swiglu_forward_quant, which
+// quantises h with the abs-max the forward recorded.
 //
 // Design: SM pairs.  The grid is a set of 2-CTA clusters, one CTA per SM,
 // persistent over 256 x 256 output tiles.  Each tile is one chain of
@@ -71,11 +75,16 @@ constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t((2
 
 __device__ unsigned int g_status;
 
+// Epilogue forms
+constexpr int EPI_BF16 = 0;          // out = bf16(scaled accumulator)
+constexpr int EPI_SWIGLU = 1;        // h = bf16(silu(g) * u), abs-max recorded
+constexpr int EPI_SWIGLU_E4M3 = 2;   // hq = e4m3(h * 448 / given abs-max)
+
 struct GemmArgs {
-  uint16_t* out;
+  void* out;
   const float* a_scale;
   const float* w_scale;
-  float* amax;
+  float* amax;   // SwiGLU: stats_h {abs_max, scale}
   int M, N, K;   // N: output columns (SwiGLU: H)
   int H;         // SwiGLU: first up row of W1
   int tiles_m, tiles_n, num_tiles, num_kb;
@@ -221,7 +230,7 @@ QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
   nb = r / gsize;
 }
 
-template <bool SWIGLU>
+template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs args) {
@@ -246,6 +255,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto tempty_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 4);
 
+  constexpr bool SWIGLU = EPI != EPI_BF16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();
   const int pair = int(cluster_id_x()), num_pairs = int(num_clusters_x());
@@ -349,6 +359,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = int(rank) * BM + q * 32 + lane;
     const float scale = args.a_scale[0] * args.w_scale[0];
     float amax = 0.0f;
+    // EPI_SWIGLU_E4M3: quantise h with the given abs-max, as quantize_with_abs_max
+    // does (fp32 product with 448 / abs_max, nearest even, saturating)
+    float qinv = 0.0f;
+    bool qzero = true;
+    if (EPI == EPI_SWIGLU_E4M3) {
+      const float given = args.amax[0];
+      qzero = !(given > 0.0f);
+      qinv = qzero ? 0.0f : 448.0f / given;
+      if (blockIdx.x == 0 && threadIdx.x == 64) args.amax[1] = qzero ? 1.0f : given / 448.0f;
+    }
     int local = 0;
     for (int tile = pair; tile < args.num_tiles; tile += num_pairs, ++local) {
       const int acc = local & 1;
@@ -361,7 +381,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool row_ok = row < args.M;
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
       if (!SWIGLU) {
-        uint16_t* orow = args.out + size_t(row) * size_t(args.N);
+        uint16_t* orow = static_cast<uint16_t*>(args.out) + size_t(row) * size_t(args.N);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           uint32_t v[32];
@@ -379,7 +399,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else {
-        uint16_t* hrow = args.out + size_t(row) * size_t(args.N) + size_t(nb) * 128;
+        const size_t hoff = size_t(row) * size_t(args.N) + size_t(nb) * 128;
+        uint16_t* hrow = static_cast<uint16_t*>(args.out) + hoff;
+        uint8_t* qrow = static_cast<uint8_t*>(args.out) + hoff;
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t g[32], u[32];
@@ -392,12 +414,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const float u0 = round_bf16(__uint_as_float(u[2 * j]) * scale);
             const float u1 = round_bf16(__uint_as_float(u[2 * j + 1]) * scale);
             p[j] = pack_bf16x2(silu_mul_f32(g0, u0), silu_mul_f32(g1, u1));
-            if (row_ok) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
+            if (EPI == EPI_SWIGLU && row_ok)
+              amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
           }
-          if (row_ok) {
+          if (EPI == EPI_SWIGLU && row_ok) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               stg16(hrow + c0 + 8 * j, make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
+          }
+          if (EPI == EPI_SWIGLU_E4M3 && row_ok) {
+            uint32_t c[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint16_t lo = qzero ? uint16_t(0)
+                                        : f32x2_to_e4m3x2(bf16_lo(p[2 * j]) * qinv, bf16_hi(p[2 * j]) * qinv);
+              const uint16_t hi = qzero ? uint16_t(0)
+                                        : f32x2_to_e4m3x2(bf16_lo(p[2 * j + 1]) * qinv,
+                                                          bf16_hi(p[2 * j + 1]) * qinv);
+              c[j] = uint32_t(lo) | (uint32_t(hi) << 16);
+            }
+            stg16(qrow + c0, make_uint4(c[0], c[1], c[2], c[3]));
+            stg16(qrow + c0 + 16, make_uint4(c[4], c[5], c[6], c[7]));
           }
         }
       }
@@ -405,7 +442,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
     }
-    if (SWIGLU) {
+    if (EPI == EPI_SWIGLU) {
       amax = warp_max(amax);
       if (lane == 0) atomic_max_nonneg(args.amax, amax);
     }
@@ -454,7 +491,7 @@ bool make_map(CUtensorMap* map, const uint8_t* ptr, int64_t rows, int64_t k) {
 
 // Number of 2-CTA clusters of this kernel that fit on the device at once
 // (cached per device and form).
-template <bool SWIGLU>
+template <int EPI>
 cudaError_t max_pairs(int* pairs) {
   static int cached[64] = {0};
   int dev = 0;
@@ -464,7 +501,7 @@ cudaError_t max_pairs(int* pairs) {
     *pairs = cached[dev];
     return cudaSuccess;
   }
-  e = cudaFuncSetAttribute(gemm_fp8_kernel<SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -479,7 +516,7 @@ cudaError_t max_pairs(int* pairs) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<SWIGLU>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
   if (dev >= 0 && dev < 64) cached[dev] = n;
@@ -487,10 +524,10 @@ cudaError_t max_pairs(int* pairs) {
   return cudaSuccess;
 }
 
-template <bool SWIGLU>
+template <int EPI>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s) {
   int pairs = 0;
-  cudaError_t e = max_pairs<SWIGLU>(&pairs);
+  cudaError_t e = max_pairs<EPI>(&pairs);
   if (e != cudaSuccess) return e;
   if (a.num_tiles < pairs) pairs = a.num_tiles;
   cudaLaunchConfig_t cfg = {};
@@ -505,7 +542,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<SWIGLU>, ma, mb, a);
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI>, ma, mb, a);
 }
 
 }  // namespace
@@ -529,8 +566,31 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.tiles_n = int((N + BN - 1) / BN);
   a.num_tiles = a.tiles_m * a.tiles_n;
   a.num_kb = int((K + BK - 1) / BK);
-  return launch<false>(ma, mb, a, s);
+  return launch<EPI_BF16>(ma, mb, a, s);
 }
+
+namespace {
+// Tensor maps and arguments shared by the two SwiGLU forms.
+bool swiglu_args(GemmArgs* a, CUtensorMap* ma, CUtensorMap* mb, void* out, float* stats_h,
+                 const uint8_t* A, const float* a_scale, const uint8_t* W1, const float* w_scale,
+                 int64_t M, int64_t H, int64_t K) {
+  if (!make_map(ma, A, M, K) || !make_map(mb, W1, 2 * H, K)) return false;
+  *a = GemmArgs{};
+  a->out = out;
+  a->a_scale = a_scale;
+  a->w_scale = w_scale;
+  a->amax = stats_h;
+  a->M = int(M);
+  a->N = int(H);
+  a->K = int(K);
+  a->H = int(H);
+  a->tiles_m = int((M + 2 * BM - 1) / (2 * BM));
+  a->tiles_n = int(H / 128);
+  a->num_tiles = a->tiles_m * a->tiles_n;
+  a->num_kb = int((K + BK - 1) / BK);
+  return true;
+}
+}  // namespace
 
 cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, const float* a_scale,
                                const uint8_t* W1, const float* w_scale, int64_t M, int64_t H,
@@ -538,21 +598,22 @@ cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, co
   cudaError_t e = cudaMemsetAsync(stats_h, 0, sizeof(float), s);
   if (e != cudaSuccess || M == 0) return e;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, M, K) || !make_map(&mb, W1, 2 * H, K)) return cudaErrorInvalidValue;
-  GemmArgs a{};
-  a.out = h;
-  a.a_scale = a_scale;
-  a.w_scale = w_scale;
-  a.amax = stats_h;
-  a.M = int(M);
-  a.N = int(H);
-  a.K = int(K);
-  a.H = int(H);
-  a.tiles_m = int((M + 2 * BM - 1) / (2 * BM));
-  a.tiles_n = int(H / 128);
-  a.num_tiles = a.tiles_m * a.tiles_n;
-  a.num_kb = int((K + BK - 1) / BK);
-  return launch<true>(ma, mb, a, s);
+  GemmArgs a;
+  if (!swiglu_args(&a, &ma, &mb, h, stats_h, A, a_scale, W1, w_scale, M, H, K))
+    return cudaErrorInvalidValue;
+  return launch<EPI_SWIGLU>(ma, mb, a, s);
+}
+
+cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* A,
+                                     const float* a_scale, const uint8_t* W1, const float* w_scale,
+                                     int64_t M, int64_t H, int64_t K, cudaStream_t s) {
+  // no rows: only the scale word is written (the elementwise form with N = 0)
+  if (M == 0) return launch_swiglu_requant(hq, stats_h, nullptr, 0, H, s);
+  CUtensorMap ma, mb;
+  GemmArgs a;
+  if (!swiglu_args(&a, &ma, &mb, hq, stats_h, A, a_scale, W1, w_scale, M, H, K))
+    return cudaErrorInvalidValue;
+  return launch<EPI_SWIGLU_E4M3>(ma, mb, a, s);
 }
 
 cudaError_t gemm_take_status(unsigned int* status) {

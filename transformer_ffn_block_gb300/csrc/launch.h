@@ -39,6 +39,11 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
 cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, const float* a_scale,
                                const uint8_t* W1, const float* w_scale, int64_t M, int64_t H,
                                int64_t K, cudaStream_t s);
+// hq[M,H] = e4m3(h * 448 / stats_h[0]) for the h of launch_gemm_swiglu, with
+// the abs-max given (not recorded); writes stats_h[1] = scale.
+cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* A,
+                                     const float* a_scale, const uint8_t* W1, const float* w_scale,
+                                     int64_t M, int64_t H, int64_t K, cudaStream_t s);
 // Reads and clears the GEMM kernels' device status word of the current device.
 cudaError_t gemm_take_status(unsigned int* status);
 
