@@ -339,6 +339,44 @@ def bench_prefill(q, torch, device, steps, warmup, dist, peaks):
         "hbm_peak_gbs": hbm,
     }
     res["down_gemm_tflops"] = 2 * N * H * C / (stage_ms[4] * 1e-3) / 1e12
+
+    # ---- the recompute form: the same chain re-run with the abs-maxes the
+    # forward recorded (4 launches; the gate|up epilogue writes E4M3 h directly)
+    st_rec = d["stats"].clone()
+
+    def recompute():
+        q.qffn_forward_recompute(d["res_out"], d["out"], d["rstd"], st_rec[0:2], st_rec[2:4],
+                                 d["res"], d["x"], d["gain"], cfg.eps, d["w1"], d["w1_scale"],
+                                 d["w2"], d["w2_scale"], cfg.B, cfg.T, C, H, d["ws"], stream=stream)
+
+    for _ in range(warmup):
+        recompute()
+    torch.cuda.synchronize()
+    r0 = torch.cuda.Event(enable_timing=True)
+    r1 = torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for _ in range(steps):
+        recompute()
+    r1.record(stream)
+    torch.cuda.synchronize()
+    ms_rec = r0.elapsed_time(r1) / steps
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(steps):
+        q.qffn_gate_up_swiglu_quant(d["hq"], st_rec[2:4], d["yq"], st_rec[1:2], d["w1"],
+                                    d["w1_scale"], N, C, H, stream=stream)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    q.qffn_check_status(stream)
+    ms_gq = g0.elapsed_time(g1) / steps
+    res["recompute"] = {
+        "what": "qffn_forward_recompute: the chain with the recorded abs-maxes given "
+                "(no bf16 h, no requantisation pass)",
+        "ms_per_step": ms_rec, "tflops": flop / (ms_rec * 1e-3) / 1e12, "launches_per_step": 4,
+        "gate_up_swiglu_e4m3_gemm_ms": ms_gq,
+        "gate_up_swiglu_e4m3_gemm_tflops": gate_up_flop / (ms_gq * 1e-3) / 1e12,
+    }
     return res
 
 
@@ -388,6 +426,20 @@ def bench_decode(q, torch, device, iters, dist, peaks):
     torch.cuda.synchronize()
     n_calls = reps * copies
     us_graph = max_over_ranks(dist, t0.elapsed_time(t1)) * 1e3 / n_calls
+    # the same calls launched eagerly back to back (each call's dual GEMV is a
+    # programmatic dependent launch of the previous call's down GEMV)
+    e_calls = reps * copies
+    for i in range(copies):
+        call(sets[i])
+    torch.cuda.synchronize()
+    t2 = torch.cuda.Event(enable_timing=True)
+    t3 = torch.cuda.Event(enable_timing=True)
+    t2.record(stream)
+    for i in range(e_calls):
+        call(sets[i % copies])
+    t3.record(stream)
+    torch.cuda.synchronize()
+    us_eager = max_over_ranks(dist, t2.elapsed_time(t3)) * 1e3 / e_calls
     # ungraphed, with per-kernel events (dual GEMV is the dominant kernel)
     g = ws[:2 * H].view(torch.int16)
     u = ws[(2 * H + 255) // 256 * 256:].view(torch.int16)
@@ -414,6 +466,8 @@ def bench_decode(q, torch, device, iters, dist, peaks):
         "metric": DECODE_METRIC, "unit": "GB/s", "value": gbs, "us_per_call": us_graph,
         "bytes_per_call": cfg.weight_bytes, "calls": n_calls, "graph": True,
         "ungraphed_us_per_call": ungraphed_us, "weight_copies_rotated": copies,
+        "eager_back_to_back_us_per_call": us_eager,
+        "eager_back_to_back_gbs": cfg.weight_bytes / (us_eager * 1e-6) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "gemv_kernel<dual> (gate+up GEMV)",
                      "achieved": dual_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": dual_gbs / peaks["hbm_gbs"], "traffic": TRAFFIC_DUAL_GEMV_BYTES,
@@ -422,7 +476,7 @@ def bench_decode(q, torch, device, iters, dist, peaks):
         "stage_us": {"gemv_dual": dual_us, "gemv_down": down_us},
         "frac_of_peak": gbs / peaks["hbm_gbs"],
         "frac_of_8tbs": gbs / 8000.0,
-        "gpu_launches": 2 * n_calls,        # dual GEMV (+silu_mul) and down GEMV
+        "gpu_launches": 2 * n_calls,        # dual GEMV (+silu_mul) and down GEMV, graph region
     }
 
 
@@ -589,6 +643,7 @@ def main():
         "stages_ms": pre["stage_ms"],
         "elementwise_gbs": pre["elementwise_gbs"],
         "down_gemm_tflops": pre["down_gemm_tflops"],
+        "recompute": pre["recompute"],
         "decode": dec,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
