@@ -225,6 +225,18 @@ qffn_status qffn_gemv_dual(uint16_t* g, uint16_t* u, const uint16_t* x, const ui
 qffn_status qffn_gemv(uint16_t* out, const uint16_t* x, const uint8_t* w, const float* row_scale,
                       int64_t rows, int64_t cols, qffn_stream_t stream);
 
+/* ---- Step A8, fused-SiLU-input arm ---------------------------------------
+ * [metrale] w8a16_gemv_silu_input(gate_out, up_out, down weights, row_scale,
+ * output): the down GEMV forms its input h = bf16(silu(g) * u) itself.
+ *   out[r] = bf16(row_scale[r] * sum_k W[r,k] * h[k])
+ * h is formed once per CTA while the input vector is staged in shared
+ * memory.  The result is bit-identical to qffn_silu_mul(g, u) followed by
+ * qffn_gemv, and g and u are not modified.  W [rows, cols] E4M3; g, u [cols]
+ * bf16.  cols % 16 == 0, 16 <= cols <= 32768, rows >= 1. */
+qffn_status qffn_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint16_t* u,
+                                 const uint8_t* w, const float* row_scale, int64_t rows,
+                                 int64_t cols, qffn_stream_t stream);
+
 /* ---- Step A7: silu_mul, in place ------------------------------------------
  * [metrale] silu_mul(gate_out, up_out -> gate_out): g[i] = bf16(silu(g[i]) * u[i]).
  * n >= 0, n % 8 == 0. */

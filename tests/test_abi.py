@@ -123,6 +123,9 @@ def test_decode_checks(lib):
     assert f(A, MIS, A, A, A, A, A, A, 4096, 14336, A, ws, None) == 3
     assert _call(lib, "qffn_gemv", A, A, A, A, 10, 24, None) == 2
     assert _call(lib, "qffn_silu_mul", A, A, 12, None) == 2
+    assert _call(lib, "qffn_gemv_silu_input", A, A, A, A, A, 10, 24, None) == 2
+    assert _call(lib, "qffn_gemv_silu_input", A, A, NULL, A, A, 10, 32, None) == 1
+    assert _call(lib, "qffn_gemv_silu_input", A, A, MIS, A, A, 10, 32, None) == 3
     assert _call(lib, "qffn_quantize_rows", A, A, A, 3, 8, None) == 2
 
 

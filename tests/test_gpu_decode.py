@@ -103,3 +103,20 @@ def test_decode_in_cuda_graph(q):
         graph.replay()
     sync()
     assert torch.equal(out2, out)
+
+
+@pytest.mark.parametrize("C,H", [(4096, 14336), (256, 768), (16, 16)])
+def test_decode_fused_silu_input_arm_bit_identical(q, C, H):
+    """Fused-SiLU-input arm (dual GEMV, then the down GEMV forming silu(g)*u from g and
+    u itself) gives the bits of the split-SiLU decode and leaves g and u untouched."""
+    cfg = DECODE["llama3-8b-decode"] if (C, H) == (4096, 14336) else DecodeConfig("f", C=C, H=H, seed=C * 3 + H)
+    di, recs, out, ws, x = run_decode(q, cfg)
+    g = empty_bf16(cfg.H)
+    u = empty_bf16(cfg.H)
+    q.qffn_gemv_dual(g, u, x, *recs["w_gate"], *recs["w_up"], cfg.H, cfg.C)
+    g0, u0 = g.clone(), u.clone()
+    o2 = empty_bf16(cfg.C)
+    q.qffn_gemv_silu_input(o2, g, u, *recs["w_down"], cfg.C, cfg.H)
+    sync()
+    assert torch.equal(o2, out)
+    assert torch.equal(g, g0) and torch.equal(u, u0)

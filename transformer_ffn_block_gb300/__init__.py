@@ -23,7 +23,7 @@ __all__ = [
     "qffn_swiglu_forward_quant", "qffn_gate_up_swiglu_quant",
     "qffn_forward_workspace_size", "qffn_forward_workspace_offsets", "qffn_forward",
     "qffn_forward_recompute",
-    "qffn_gemv_dual", "qffn_gemv", "qffn_silu_mul", "qffn_decode_workspace_size",
+    "qffn_gemv_dual", "qffn_gemv", "qffn_gemv_silu_input", "qffn_silu_mul", "qffn_decode_workspace_size",
     "qffn_decode_forward", "qffn_decode_forward_noalloc",
 ]
 
@@ -64,6 +64,7 @@ _SIGS = {
                                 _I64, _I64, _I64, _I64, _P, _SZ, _P], _S),
     "qffn_gemv_dual": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], _S),
     "qffn_gemv": ([_P, _P, _P, _P, _I64, _I64, _P], _S),
+    "qffn_gemv_silu_input": ([_P, _P, _P, _P, _P, _I64, _I64, _P], _S),
     "qffn_silu_mul": ([_P, _P, _I64, _P], _S),
     "qffn_decode_workspace_size": ([_I64, _I64], _SZ),
     "qffn_decode_forward": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P], _S),
@@ -204,6 +205,12 @@ def qffn_gemv_dual(g, u, x, w_gate, s_gate, w_up, s_up, H, C, stream=None):
 def qffn_gemv(out, x, w, row_scale, rows, cols, stream=None):
     _check("qffn_gemv", lib.qffn_gemv(
         _ptr(out), _ptr(x), _ptr(w), _ptr(row_scale), int(rows), int(cols), _stream(stream)))
+
+
+def qffn_gemv_silu_input(out, g, u, w, row_scale, rows, cols, stream=None):
+    _check("qffn_gemv_silu_input", lib.qffn_gemv_silu_input(
+        _ptr(out), _ptr(g), _ptr(u), _ptr(w), _ptr(row_scale), int(rows), int(cols),
+        _stream(stream)))
 
 
 def qffn_silu_mul(g, u, n, stream=None):

@@ -306,6 +306,17 @@ qffn_status qffn_gemv(uint16_t* out, const uint16_t* x, const uint8_t* w, const 
                                      false, stream));
 }
 
+qffn_status qffn_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint16_t* u,
+                                 const uint8_t* w, const float* row_scale, int64_t rows,
+                                 int64_t cols, qffn_stream_t stream) {
+  QFFN_PTR(out); QFFN_PTR(g); QFFN_PTR(u); QFFN_PTR(w); QFFN_PTR(row_scale);
+  QFFN_REQUIRE(rows >= 1 && cols >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(cols % 16 == 0 && cols >= 16 && cols <= 32768 && rows <= kMaxRows,
+               QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(g); QFFN_ALIGNED(u); QFFN_ALIGNED(w); QFFN_ALIGNED4(row_scale);
+  return from_cuda(qffn::launch_gemv_silu_input(out, g, u, w, row_scale, rows, cols, stream));
+}
+
 qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream_t stream) {
   QFFN_PTR(g); QFFN_PTR(u);
   QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);

@@ -16,6 +16,11 @@
 // code for the single and the dual form, so they agree bit for bit; the dual
 // form reads x once for the gate and the up row of the same index.
 //
+// The fused-SiLU-input arm's down GEMV (w8a16_gemv_silu_input) reads g and u
+// and forms h = bf16(silu(g) * u) while staging its input vector in shared
+// memory, once per CTA, with the arithmetic of silu_mul; its output is the
+// same as silu_mul followed by the plain GEMV.
+//
 // In the decode the dual GEMV applies silu_mul where g and u are produced and
 // leaves h = bf16(silu(g) * u) in the gate buffer (the split-SiLU arm's
 // buffer use); the down GEMV on h is a programmatic dependent launch whose
@@ -54,7 +59,8 @@ QFFN_DEVI void dot16(uint4 w, uint4 xa, uint4 xb, uint64_t& acc) {
 
 struct Gemv {
   uint16_t* out[2];
-  const uint16_t* x;         // input bf16 [cols]
+  const uint16_t* x;         // input bf16 [cols] (SILU_IN: the gate vector g)
+  const uint16_t* x_up;      // SILU_IN: the up vector u; input = bf16(silu(g) * u)
   const uint8_t* w[2];
   const float* s[2];
   int rows, cols;
@@ -63,7 +69,7 @@ struct Gemv {
 // SILU (dual only): the gate output slot receives h = bf16(silu(g) * u)
 // instead of g -- the decode's silu_mul applied where g and u are produced,
 // as the split-SiLU arm leaves h in the gate buffer.
-template <bool DUAL, bool SILU, int TPR>
+template <bool DUAL, bool SILU, int TPR, bool SILU_IN = false>
 __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
   constexpr int kU = DUAL ? kUDual : kUSingle;
   extern __shared__ uint4 xs[];
@@ -98,7 +104,9 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
   }
   pdl_wait();                        // x may come from the preceding kernel
   pdl_trigger();
-  for (int i = threadIdx.x; i < nvec; i += kThreads) xs[i] = ld16_once(G.x + size_t(i) * 8);
+  for (int i = threadIdx.x; i < nvec; i += kThreads)
+    xs[i] = SILU_IN ? swiglu8(ld16_once(G.x + size_t(i) * 8), ld16_once(G.x_up + size_t(i) * 8))
+                    : ld16_once(G.x + size_t(i) * 8);
   __syncthreads();
 
   for (int base = blockIdx.x * RPB; base < rows; base += gridDim.x * RPB) {
@@ -170,10 +178,10 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
   }
 }
 
-template <bool DUAL, bool SILU, int TPR>
+template <bool DUAL, bool SILU, int TPR, bool SILU_IN = false>
 cudaError_t launch_t(const Gemv& G, bool pdl, cudaStream_t s) {
   const size_t smem = size_t(G.cols) * 2;
-  auto fn = gemv_kernel<DUAL, SILU, TPR>;
+  auto fn = gemv_kernel<DUAL, SILU, TPR, SILU_IN>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
@@ -222,6 +230,21 @@ cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const
   G.rows = int(rows);
   G.cols = int(cols);
   return w1 != nullptr ? launch_d<true, false>(G, pdl, s) : launch_d<false, false>(G, pdl, s);
+}
+
+cudaError_t launch_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint16_t* u,
+                                   const uint8_t* w, const float* row_scale, int64_t rows,
+                                   int64_t cols, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  Gemv G{};
+  G.out[0] = out;
+  G.x = g;
+  G.x_up = u;
+  G.w[0] = w;
+  G.s[0] = row_scale;
+  G.rows = int(rows);
+  G.cols = int(cols);
+  return launch_t<false, false, 32, true>(G, false, s);
 }
 
 cudaError_t launch_decode(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,

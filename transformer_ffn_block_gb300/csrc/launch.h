@@ -52,6 +52,11 @@ cudaError_t gemm_take_status(unsigned int* status);
 cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const uint8_t* w0,
                         const float* s0, const uint8_t* w1, const float* s1, int64_t rows,
                         int64_t cols, bool pdl, cudaStream_t s);
+// out[r] = bf16(s[r] * W[r,:] . h) with h = bf16(silu(g) * u) formed while the
+// input vector is staged (the fused-SiLU-input arm's down GEMV).
+cudaError_t launch_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint16_t* u,
+                                   const uint8_t* w, const float* row_scale, int64_t rows,
+                                   int64_t cols, cudaStream_t s);
 // The whole decode FFN: the dual GEMV (g, u), then the down GEMV on
 // h = bf16(silu(g) * u) formed in its prologue, launched as a programmatic
 // dependent launch so its first weight loads overlap the dual GEMV's tail.
