@@ -14,7 +14,8 @@ It is a plain, slow, float64 restatement of what the pages compute:
 * ``ffn``     -- the prefill chain (fused residual + RMSNorm + abs-max,
   per-tensor quantisation, scaled FP8 GEMMs, SwiGLU with abs-max and
   requantisation), its recompute form with the activation abs-maxes given
-  (``swiglu_forward_quant``, ``ffn_forward_recompute``), and the single-token
+  (``swiglu_forward_quant``, ``ffn_forward_recompute``), the generic
+  quantise-then-matmul of the attention projections (``qmm``), and the single-token
   decode FFN (dual row-scaled GEMV, silu_mul, down GEMV).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against hand-worked
@@ -25,13 +26,13 @@ from .codecs import (E4M3_MAX, bf16_to_f32, bf16_to_f64, e4m3_decode, e4m3_encod
                      e4m3_to_scaled_int, f32_to_bf16, f64_to_bf16)
 from .ffn import (absmax, decode_forward, ffn_forward, ffn_forward_recompute, fp8_gemm_scaled,
                   gemv_dual, gemv_row_scaled, quantize_rows, quantize_tensor,
-                  quantize_with_abs_max, residual_rmsnorm_absmax, rmsnorm_f64, silu_f64,
+                  quantize_with_abs_max, qmm, residual_rmsnorm_absmax, rmsnorm_f64, silu_f64,
                   silu_mul, swiglu, swiglu_forward_quant, swiglu_quant)
 
 __all__ = [
     "E4M3_MAX", "bf16_to_f32", "bf16_to_f64", "e4m3_decode", "e4m3_encode",
     "e4m3_to_scaled_int", "f32_to_bf16", "f64_to_bf16", "absmax", "decode_forward",
     "ffn_forward", "ffn_forward_recompute", "fp8_gemm_scaled", "gemv_dual", "gemv_row_scaled", "quantize_rows",
-    "quantize_tensor", "quantize_with_abs_max", "residual_rmsnorm_absmax", "rmsnorm_f64",
+    "quantize_tensor", "quantize_with_abs_max", "qmm", "residual_rmsnorm_absmax", "rmsnorm_f64",
     "silu_f64", "silu_mul", "swiglu", "swiglu_forward_quant", "swiglu_quant",
 ]

@@ -40,6 +40,8 @@ R11 the SwiGLU-with-quantisation result equals swiglu (recording the abs-max
     of bf16 h) followed by quantisation of that same bf16 h.
 R14 decode g, u, h are bf16; the row scale multiplies the finished sum.
 R15 the decode input is already normalised; no norm in the decode FFN.
+R19 a matmul bias (the QKV projection's) is added to the scaled accumulator
+    before its single rounding to bf16.
 
 Precision: RMSNorm, SwiGLU and GEMV sums are float64 with one final rounding
 to bf16; scales are IEEE fp32 divisions; the FP8 GEMM is exact (see
@@ -170,6 +172,30 @@ def fp8_gemm_scaled(a_codes, a_scale, w_codes, w_scale):
         raise ValueError("K above 2**15 breaks the exact-sum bound")
     acc = a @ w.T
     return f64_to_bf16(np.ldexp(acc, -18) * float(np.float32(a_scale)) * float(np.float32(w_scale)))
+
+
+def qmm(in_bits, amax, w_codes, w_scale, bias_bits=None):
+    """``forward_qmm``: quantise a bf16 activation with its recorded abs-max, then
+    the scaled FP8 matmul, with an optional bf16 bias per output column.
+
+    [llmq-model] ``forward_qmm(out, inp, weight, bias, ...)`` runs
+    ``quantize_with_abs_max`` on ``inp`` and then ``matmul(out, weight,
+    inp.Quant, bias, weight.scale(), inp.Quant.scale(), ...)``.
+    ``_forward_block`` calls it for the QKV projection (with
+    ``Attn_QKV_b``), the attention output projection and both FFN
+    projections.  R9: the exact accumulator times both scales is rounded once
+    to bf16.  R19: a bias is added to that scaled value before the one
+    rounding.  Returns ``(out bits [M, N], codes [M, K], scale)``.
+    """
+    codes, scale = quantize_with_abs_max(in_bits, amax)
+    a = e4m3_to_scaled_int(codes)
+    w = e4m3_to_scaled_int(w_codes)
+    if a.shape[-1] > (1 << 15):
+        raise ValueError("K above 2**15 breaks the exact-sum bound")
+    v = np.ldexp(a @ w.T, -18) * float(scale) * float(np.float32(w_scale))
+    if bias_bits is not None:
+        v = v + bf16_to_f64(bias_bits)[None, :]
+    return f64_to_bf16(v), codes, scale
 
 
 # ------------------------------------------------------------------ A4 (K5/K6)

@@ -169,6 +169,18 @@ def gemm(a_codes, a_scale, w_codes, w_scale):
     return out
 
 
+def gemm_bias(a_codes, a_scale, w_codes, w_scale, bias_bits):
+    """out[m][n] = bf16(sa * sw * sum_k A[m][k] * W[n][k] + bias[n]), exact sums, one rounding."""
+    sa, sw = Fraction(float(a_scale)), Fraction(float(w_scale))
+    bias = [bf16_value(b) for b in bias_bits]
+    out = []
+    for arow in a_codes:
+        av = [e4m3_value(c) for c in arow]
+        out.append([round_bf16(sum(x * e4m3_value(c) for x, c in zip(av, wrow)) * sa * sw + b)
+                    for wrow, b in zip(w_codes, bias)])
+    return out
+
+
 def silu_times(g_bits: int, u_bits: int) -> int:
     g = Decimal(bf16_value(g_bits).numerator) / Decimal(bf16_value(g_bits).denominator)
     u = bf16_value(u_bits)

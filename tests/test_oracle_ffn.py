@@ -380,3 +380,36 @@ def test_recompute_tiny_brute_force_chain():
     assert o["hq"].tolist() == [hq[i * H:(i + 1) * H] for i in range(N)]
     assert Fraction(float(o["stats_h"][1])) == sh
     assert o["out"].tolist() == brute.gemm(o["hq"].tolist(), float(sh), w2q.tolist(), w2s)
+
+
+# ------------------------------------------------------------------ forward_qmm (attention projections)
+def test_qmm_matches_brute_force_with_bias():
+    """Quantise with the recorded abs-max, scaled FP8 matmul, bias before the one rounding."""
+    M, K, N = 3, 24, 5
+    x = _mixed_bf16((M, K), 111)
+    amax = oracle.absmax(x)
+    wq, ws = oracle.quantize_tensor(random_bf16((N, K), 112, std=0.02))
+    bias = _mixed_bf16((N,), 113)
+    out, codes, scale = oracle.qmm(x, amax, wq, ws, bias)
+    bq, bs = brute.quantize(list(x.ravel()), float(amax))
+    assert list(codes.ravel()) == bq and Fraction(float(scale)) == bs
+    rows = [bq[i * K:(i + 1) * K] for i in range(M)]
+    assert out.tolist() == brute.gemm_bias(rows, float(bs), wq.tolist(), ws, list(bias))
+    # no bias: the plain scaled matmul of the same codes
+    out0, _, _ = oracle.qmm(x, amax, wq, ws)
+    assert out0.tolist() == brute.gemm(rows, float(bs), wq.tolist(), ws)
+    assert not np.array_equal(out0, out)
+
+
+def test_qmm_identity_weight_closed_form():
+    """W = 448 * I with scale 1/448: out = bf16(dequant(q) * scale + bias)."""
+    K = 32
+    x = _mixed_bf16((4, K), 114)
+    amax = oracle.absmax(x)
+    w = np.zeros((K, K), np.uint8)
+    np.fill_diagonal(w, 0x7E)
+    bias = _mixed_bf16((K,), 115)
+    out, codes, scale = oracle.qmm(x, amax, w, np.float32(1 / 448.0), bias)
+    want = oracle.f64_to_bf16(oracle.e4m3_decode(codes) * float(scale) * 448.0 * float(np.float32(1 / 448.0))
+                              + oracle.bf16_to_f64(bias)[None, :])
+    np.testing.assert_array_equal(out, want)
