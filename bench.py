@@ -380,6 +380,71 @@ def bench_prefill(q, torch, device, steps, warmup, dist, peaks):
     return res
 
 
+def bench_attention_projections(q, torch, device, steps, warmup):
+    """The attention-side uses of the same primitives at the Llama-3-8B shape:
+    LN1 (fused residual + RMSNorm + abs-max) into the QKV projection
+    (N x 4096 -> N x 6144, forward_qmm), and the abs-max of the attention output
+    into the output projection (N x 4096 -> N x 4096).  The attention output is
+    a synthetic N(0,1) stand-in; weights are N(0, 0.02) quantised on the GPU."""
+    from ffn_inputs import random_bf16
+    cfg = PREFILL_CFG
+    N, C = cfg.N, cfg.C
+    nqkv = C + 2 * 1024                      # 32 query heads + 2 x 8 key/value heads of 128
+    inp = prefill_inputs(cfg)
+    res, x, gain = (to_dev(inp[k], torch, device) for k in ("res", "x", "gain"))
+    att = to_dev(random_bf16((N, C), seed=301), torch, device)
+    wst = torch.zeros(4, dtype=torch.float32, device=device)
+    wqkv = torch.empty(nqkv, C, dtype=torch.uint8, device=device)
+    wo = torch.empty(C, C, dtype=torch.uint8, device=device)
+    for w, seed, st in ((wqkv, 302, wst[0:2]), (wo, 303, wst[2:4])):
+        wb = to_dev(random_bf16(tuple(w.shape), seed=seed, std=0.02), torch, device)
+        q.qffn_absmax(st, wb, wb.numel())
+        q.qffn_quantize(w, st, wb, wb.numel())
+        del wb
+    r = torch.empty(N, C, dtype=torch.int16, device=device)
+    y = torch.empty(N, C, dtype=torch.int16, device=device)
+    rstd = torch.empty(N, dtype=torch.float32, device=device)
+    st = torch.zeros(4, dtype=torch.float32, device=device)
+    qbuf = torch.empty(N, C, dtype=torch.uint8, device=device)
+    qkv = torch.empty(N, nqkv, dtype=torch.int16, device=device)
+    atto = torch.empty(N, C, dtype=torch.int16, device=device)
+    stream = torch.cuda.Stream(device)
+
+    def ln1():
+        q.qffn_rmsnorm_absmax(r, y, rstd, st[0:2], res, x, gain, cfg.eps, N, C, stream=stream)
+
+    def qkv_proj():
+        q.qffn_qmm(qkv, qbuf, st[0:2], y, None, wqkv, wst[1:2], N, nqkv, C, stream=stream)
+
+    def out_proj():
+        q.qffn_absmax(st[2:4], att, N * C, stream=stream)
+        q.qffn_qmm(atto, qbuf, st[2:4], att, None, wo, wst[3:4], N, C, C, stream=stream)
+
+    out = {}
+    for name, fn in (("ln1", ln1), ("qkv_qmm", qkv_proj), ("out_proj", out_proj)):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        out[name] = a.elapsed_time(b) / steps
+    q.qffn_check_status(stream)
+    f_qkv = 2.0 * N * nqkv * C
+    f_o = 2.0 * N * C * C
+    return {
+        "workload": f"llama3-8b attention projections: N={N}, C={C}, QKV out {nqkv}",
+        "ln1_ms": out["ln1"], "qkv_qmm_ms": out["qkv_qmm"], "out_proj_ms": out["out_proj"],
+        "qkv_tflops": f_qkv / (out["qkv_qmm"] * 1e-3) / 1e12,
+        "out_proj_tflops": f_o / (out["out_proj"] * 1e-3) / 1e12,
+        "ln1_plus_qkv_tflops": f_qkv / ((out["ln1"] + out["qkv_qmm"]) * 1e-3) / 1e12,
+    }
+
+
 def bench_decode(q, torch, device, iters, dist, peaks):
     cfg = DECODE_CFG
     C, H = cfg.C, cfg.H
@@ -624,6 +689,7 @@ def main():
     peaks = load_peaks()
     pre = bench_prefill(q, torch, device, args.steps, args.warmup, dist, peaks)
     dec = bench_decode(q, torch, device, args.decode_iters, dist, peaks)
+    att = bench_attention_projections(q, torch, device, args.steps, args.warmup)
     cfg = PREFILL_CFG
     value = job_throughput(cfg.gemm_flop, world, pre["ms_per_step"])
     e2e_value = job_throughput(cfg.gemm_flop, world, pre["e2e_ms"])
@@ -644,6 +710,7 @@ def main():
         "elementwise_gbs": pre["elementwise_gbs"],
         "down_gemm_tflops": pre["down_gemm_tflops"],
         "recompute": pre["recompute"],
+        "attention_projections": att,
         "decode": dec,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

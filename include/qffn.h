@@ -117,6 +117,21 @@ qffn_status qffn_fp8_gemm_scaled(uint16_t* out, const uint8_t* A, const float* a
                                  const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
                                  int64_t K, qffn_stream_t stream);
 
+/* ---- forward_qmm: quantise with the recorded abs-max, then the matmul -----
+ * [llmq-model] forward_qmm(out, inp, weight, bias, ...): quantize_with_abs_max
+ * of inp, then matmul with weight.scale() and inp.Quant.scale().
+ * _forward_block uses it for the attention projections: the QKV projection of
+ * LN1 (after qffn_rmsnorm_absmax), with the optional Attn_QKV_b bias, and the
+ * output projection of the attention result (after qffn_absmax).
+ *   q[M,K]   = e4m3(in * 448 / stats[0]);  stats[1] = scale
+ *   out[M,N] = bf16(stats[1] * w_scale[0] * sum_k q[m,k] * W[n,k] + bias[n])
+ * The bias (bf16 [N], may be NULL) is added to the scaled fp32 accumulator
+ * before the one rounding.  q is caller scratch of M*K bytes, readable after
+ * the call.  Shape rules of qffn_fp8_gemm_scaled. */
+qffn_status qffn_qmm(uint16_t* out, uint8_t* q, float* stats, const uint16_t* in,
+                     const uint16_t* bias, const uint8_t* W, const float* w_scale, int64_t M,
+                     int64_t N, int64_t K, qffn_stream_t stream);
+
 /* ---- Steps A3 + A4 fused: gate|up GEMM with the SwiGLU epilogue -----------
  * [llmq-model] forward_qmm on MLP_Up_w (W1 = [2H, C], gate rows [0,H) then up
  * rows [H,2H)) followed by swiglu_forward with its abs-max.  The gate and up

@@ -156,3 +156,11 @@ def test_recompute_form_checks(lib):
     assert h(*bad) == 2
     bad = list(args); bad[17] = A + 16
     assert h(*bad) == 3
+
+
+def test_qmm_checks(lib):
+    f = lambda *a: _call(lib, "qffn_qmm", *a)
+    assert f(A, NULL, A, A, NULL, A, A, 4, 32, 16, None) == 1   # q scratch required
+    assert f(A, A, A, A, NULL, A, A, 4, 48, 16, None) == 2      # N % 32
+    assert f(A, A, A, A, NULL, A, A, 4, 32, 24, None) == 2      # K % 16
+    assert f(A, A, A, A, MIS, A, A, 4, 32, 16, None) == 3       # bias misaligned

@@ -19,7 +19,7 @@ __all__ = [
     "QffnError", "lib", "build", "LIB_PATH", "STATUS",
     "qffn_status_string", "qffn_abi_version", "qffn_check_status",
     "qffn_rmsnorm_absmax", "qffn_absmax", "qffn_quantize", "qffn_quantize_rows",
-    "qffn_fp8_gemm_scaled", "qffn_gate_up_swiglu", "qffn_swiglu_quant",
+    "qffn_fp8_gemm_scaled", "qffn_qmm", "qffn_gate_up_swiglu", "qffn_swiglu_quant",
     "qffn_swiglu_forward_quant", "qffn_gate_up_swiglu_quant",
     "qffn_forward_workspace_size", "qffn_forward_workspace_offsets", "qffn_forward",
     "qffn_forward_recompute",
@@ -52,6 +52,7 @@ _SIGS = {
     "qffn_quantize": ([_P, _P, _P, _I64, _P], _S),
     "qffn_quantize_rows": ([_P, _P, _P, _I64, _I64, _P], _S),
     "qffn_fp8_gemm_scaled": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
+    "qffn_qmm": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
     "qffn_gate_up_swiglu": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
     "qffn_swiglu_quant": ([_P, _P, _P, _P, _I64, _I64, _P], _S),
     "qffn_swiglu_forward_quant": ([_P, _P, _P, _I64, _I64, _P], _S),
@@ -140,6 +141,12 @@ def qffn_fp8_gemm_scaled(out, a, a_scale, w, w_scale, M, N, K, stream=None):
     _check("qffn_fp8_gemm_scaled", lib.qffn_fp8_gemm_scaled(
         _ptr(out), _ptr(a), _ptr(a_scale), _ptr(w), _ptr(w_scale), int(M), int(N), int(K),
         _stream(stream)))
+
+
+def qffn_qmm(out, q, stats, inp, bias, w, w_scale, M, N, K, stream=None):
+    _check("qffn_qmm", lib.qffn_qmm(
+        _ptr(out), _ptr(q), _ptr(stats), _ptr(inp), _ptr(bias), _ptr(w), _ptr(w_scale),
+        int(M), int(N), int(K), _stream(stream)))
 
 
 def qffn_gate_up_swiglu(h, stats_h, yq, y_scale, w1, w1_scale, N, C, H, stream=None):

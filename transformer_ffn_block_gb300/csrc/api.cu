@@ -138,6 +138,22 @@ qffn_status qffn_fp8_gemm_scaled(uint16_t* out, const uint8_t* A, const float* a
   return from_cuda(qffn::launch_gemm_bf16(out, A, a_scale, W, w_scale, M, N, K, stream));
 }
 
+qffn_status qffn_qmm(uint16_t* out, uint8_t* q, float* stats, const uint16_t* in,
+                     const uint16_t* bias, const uint8_t* W, const float* w_scale, int64_t M,
+                     int64_t N, int64_t K, qffn_stream_t stream) {
+  QFFN_PTR(out); QFFN_PTR(q); QFFN_PTR(stats); QFFN_PTR(in); QFFN_PTR(W); QFFN_PTR(w_scale);
+  QFFN_REQUIRE(M >= 0 && N >= 0 && K >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(M <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(N % 32 == 0 && N >= 32 && N <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(K % 16 == 0 && K >= 16 && K <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE((M + 127) / 128 * ((N + 255) / 256) < (int64_t(1) << 31), QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(out); QFFN_ALIGNED(q); QFFN_ALIGNED4(stats); QFFN_ALIGNED(in); QFFN_ALIGNED(bias);
+  QFFN_ALIGNED(W); QFFN_ALIGNED4(w_scale);
+  // quantize_with_abs_max: q, stats[1]; then the scaled matmul with the bias
+  QFFN_CUDA(qffn::launch_quantize(q, stats, in, M * K, stream));
+  return from_cuda(qffn::launch_gemm_bf16(out, q, stats + 1, W, w_scale, M, N, K, stream, bias));
+}
+
 qffn_status qffn_gate_up_swiglu(uint16_t* h, float* stats_h, const uint8_t* yq,
                                 const float* y_scale, const uint8_t* w1, const float* w1_scale,
                                 int64_t N, int64_t C, int64_t H, qffn_stream_t stream) {

@@ -1,6 +1,6 @@
 // Scaled FP8 (E4M3) GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-//   gemm_bf16   : out[M,N]  = bf16(sA*sW * A[M,K] . W[N,K]^T)
+//   gemm_bf16   : out[M,N]  = bf16(sA*sW * A[M,K] . W[N,K]^T (+ bias[N]))
 //   gemm_swiglu : h[M,H]    = bf16(silu(g)*u), g / u the bf16-rounded gate and
 //                 up products of W1 = [2H, K] (gate rows [0,H), up rows
 //                 [H,2H)); the tensor abs-max of h is recorded on the way.
@@ -85,6 +85,7 @@ struct GemmArgs {
   const float* a_scale;
   const float* w_scale;
   float* amax;   // SwiGLU: stats_h {abs_max, scale}
+  const uint16_t* bias;   // bf16 output: optional bf16 bias per output column
   int M, N, K;   // N: output columns (SwiGLU: H)
   int H;         // SwiGLU: first up row of W1
   int tiles_m, tiles_n, num_tiles, num_kb;
@@ -389,10 +390,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int col = nb * BN + c0;
           if (row_ok && col < args.N) {
             uint32_t p[16];
+            if (args.bias != nullptr) {
+              // bias added to the scaled accumulator before the one rounding
+              uint32_t bw[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              p[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * scale,
-                                 __uint_as_float(v[2 * j + 1]) * scale);
+              for (int j = 0; j < 4; ++j) {
+                const uint4 b4 = ld16_ro(args.bias + col + 8 * j);
+                bw[4 * j] = b4.x; bw[4 * j + 1] = b4.y; bw[4 * j + 2] = b4.z; bw[4 * j + 3] = b4.w;
+              }
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                p[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * scale + bf16_lo(bw[j]),
+                                   __uint_as_float(v[2 * j + 1]) * scale + bf16_hi(bw[j]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                p[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * scale,
+                                   __uint_as_float(v[2 * j + 1]) * scale);
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               stg16(orow + col + 8 * j, make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]));
@@ -549,7 +564,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
 
 cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
                              const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
-                             int64_t K, cudaStream_t s) {
+                             int64_t K, cudaStream_t s, const uint16_t* bias) {
   if (M == 0) return cudaSuccess;
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, M, K) || !make_map(&mb, W, N, K)) return cudaErrorInvalidValue;
@@ -558,6 +573,7 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.a_scale = a_scale;
   a.w_scale = w_scale;
   a.amax = nullptr;
+  a.bias = bias;
   a.M = int(M);
   a.N = int(N);
   a.K = int(K);
