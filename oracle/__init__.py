@@ -15,7 +15,8 @@ It is a plain, slow, float64 restatement of what the pages compute:
   per-tensor quantisation, scaled FP8 GEMMs, SwiGLU with abs-max and
   requantisation), its recompute form with the activation abs-maxes given
   (``swiglu_forward_quant``, ``ffn_forward_recompute``), the generic
-  quantise-then-matmul of the attention projections (``qmm``), and the single-token
+  quantise-then-matmul of the attention projections (``qmm``), the FP8 backward of
+  the FFN (``swiglu_backward``, ``backward_qmm``, ``ffn_backward``), and the single-token
   decode FFN (dual row-scaled GEMV, silu_mul, down GEMV).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against hand-worked
@@ -24,15 +25,15 @@ and brute-force exact arithmetic on tiny inputs (``tests/brute.py``).
 """
 from .codecs import (E4M3_MAX, bf16_to_f32, bf16_to_f64, e4m3_decode, e4m3_encode,
                      e4m3_to_scaled_int, f32_to_bf16, f64_to_bf16)
-from .ffn import (absmax, decode_forward, ffn_forward, ffn_forward_recompute, fp8_gemm_scaled,
-                  gemv_dual, gemv_row_scaled, quantize_rows, quantize_tensor,
+from .ffn import (absmax, backward_qmm, decode_forward, ffn_backward, ffn_forward,
+                  ffn_forward_recompute, fp8_gemm_scaled, fp8_gemm_scaled_acc, gemv_dual, gemv_row_scaled, quantize_rows, quantize_tensor,
                   quantize_with_abs_max, qmm, residual_rmsnorm_absmax, rmsnorm_f64, silu_f64,
-                  silu_mul, swiglu, swiglu_forward_quant, swiglu_quant)
+                  silu_mul, swiglu, swiglu_backward, swiglu_forward_quant, swiglu_quant)
 
 __all__ = [
     "E4M3_MAX", "bf16_to_f32", "bf16_to_f64", "e4m3_decode", "e4m3_encode",
-    "e4m3_to_scaled_int", "f32_to_bf16", "f64_to_bf16", "absmax", "decode_forward",
-    "ffn_forward", "ffn_forward_recompute", "fp8_gemm_scaled", "gemv_dual", "gemv_row_scaled", "quantize_rows",
+    "e4m3_to_scaled_int", "f32_to_bf16", "f64_to_bf16", "absmax", "backward_qmm", "decode_forward",
+    "ffn_backward", "ffn_forward", "ffn_forward_recompute", "fp8_gemm_scaled", "fp8_gemm_scaled_acc", "gemv_dual", "gemv_row_scaled", "quantize_rows",
     "quantize_tensor", "quantize_with_abs_max", "qmm", "residual_rmsnorm_absmax", "rmsnorm_f64",
-    "silu_f64", "silu_mul", "swiglu", "swiglu_forward_quant", "swiglu_quant",
+    "silu_f64", "silu_mul", "swiglu", "swiglu_backward", "swiglu_forward_quant", "swiglu_quant",
 ]

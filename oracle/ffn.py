@@ -42,6 +42,15 @@ R14 decode g, u, h are bf16; the row scale multiplies the finished sum.
 R15 the decode input is already normalised; no norm in the decode FFN.
 R19 a matmul bias (the QKV projection's) is added to the scaled accumulator
     before its single rounding to bf16.
+R20 backward: gradients are bf16 (the model dtype of the activation
+    buffers); their FP8 copies use E4M3 like the activations (the pages leave
+    the gradient FP8 type open).
+R21 swiglu_backward: with g, u the bf16 gate/up values and dh the bf16
+    gradient of h, ``dg = dh * u * sigmoid(g) * (1 + g * (1 - sigmoid(g)))``
+    and ``du = dh * silu(g)``, each rounded once to bf16; gate gradient in
+    columns ``[0, H)``, up in ``[H, 2H)``; the abs-max of both is recorded.
+R22 weight-gradient accumulation (``accumulate_gradient``): the new value is
+    ``bf16(old + scaled product)``, one rounding.
 
 Precision: RMSNorm, SwiGLU and GEMV sums are float64 with one final rounding
 to bf16; scales are IEEE fp32 divisions; the FP8 GEMM is exact (see
@@ -290,6 +299,81 @@ def ffn_forward_recompute(res_bits, x_bits, gain_bits, eps, w1_codes, w1_scale, 
         "r": r, "y": y, "rstd": rstd, "stats_y": np.array([amax_y, sy], dtype=np.float32),
         "yq": yq, "gu": gu, "hq": hq, "stats_h": np.array([amax_h, sh], dtype=np.float32),
         "out": out,
+    }
+
+
+# ------------------------------------------------------------------ FFN backward (FP8)
+def swiglu_backward(dh_bits, gu_bits, H: int):
+    """Gradient of ``h = silu(g) * u`` w.r.t. the fused up-projection output.
+
+    [llmq-model] ``_backward_block``: ``swiglu_backward(DMlpUp.Value, DSwiGLU,
+    MlpUp, DMlpUp.Quant.abs_max(), B, T, D)``.  R21: ``dg = dh * u *
+    sigmoid(g) * (1 + g * (1 - sigmoid(g)))``, ``du = dh * silu(g)`` in
+    float64, each rounded once to bf16; R1 layout (gate first).  Returns
+    ``(d_gu bits [N, 2H], abs-max fp32)``.
+    """
+    gu = np.asarray(gu_bits, dtype=np.uint16)
+    g = bf16_to_f64(gu[..., :H])
+    u = bf16_to_f64(gu[..., H:2 * H])
+    dh = bf16_to_f64(dh_bits)
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-g))
+    dg = dh * u * sig * (1.0 + g * (1.0 - sig))
+    du = dh * (g * sig)
+    d = f64_to_bf16(np.concatenate([dg, du], axis=-1))
+    return d, absmax(d)
+
+
+def fp8_gemm_scaled_acc(a_codes, a_scale, w_codes, w_scale, old_bits=None):
+    """``fp8_gemm_scaled`` with ``accumulate_gradient`` (R22): ``bf16(old + product)``."""
+    if old_bits is None:
+        return fp8_gemm_scaled(a_codes, a_scale, w_codes, w_scale)
+    a = e4m3_to_scaled_int(a_codes)
+    w = e4m3_to_scaled_int(w_codes)
+    if a.shape[-1] > (1 << 15):
+        raise ValueError("K above 2**15 breaks the exact-sum bound")
+    v = np.ldexp(a @ w.T, -18) * float(np.float32(a_scale)) * float(np.float32(w_scale))
+    return f64_to_bf16(bf16_to_f64(old_bits) + v)
+
+
+def backward_qmm(dout_bits, dout_amax, inp_codes, inp_scale, w_codes, w_scale, dw_old_bits=None):
+    """The FP8 branch of ``backward_qmm`` for one projection ``out = inp @ W^T``.
+
+    [llmq-model] ``backward_qmm``, FP8 weights: ``quantize_with_abs_max`` of
+    dout with its recorded abs-max; ``dinp = matmul(transpose(W), dout_q)``
+    with ``W.scale() * dout.scale()`` (reduction over the output channels);
+    ``dW (+)= matmul(transpose(inp_q), transpose(dout_q))`` with
+    ``inp.scale() * dout.scale()`` (reduction over the tokens), the forward's
+    quantised input reused.  Shapes: dout ``[N, OC]``, inp ``[N, IC]``,
+    W ``[OC, IC]``.  Returns ``(dinp bits [N, IC], dW bits [OC, IC], dout
+    codes, dout scale)``.
+    """
+    dq, ds = quantize_with_abs_max(dout_bits, dout_amax)
+    dinp = fp8_gemm_scaled(dq, ds, np.ascontiguousarray(np.asarray(w_codes).T), w_scale)
+    dw = fp8_gemm_scaled_acc(np.ascontiguousarray(dq.T), ds,
+                             np.ascontiguousarray(np.asarray(inp_codes).T), inp_scale, dw_old_bits)
+    return dinp, dw, dq, ds
+
+
+def ffn_backward(dout_bits, dout_amax, yq_codes, y_scale, hq_codes, h_scale, w1_codes, w1_scale,
+                 w2_codes, w2_scale, H: int, dw1_old=None, dw2_old=None):
+    """Backward of the FP8 FFN (after the norm) [llmq-model ``_backward_block``].
+
+    The down projection's ``backward_qmm`` (dout = the block-output gradient,
+    inp = the quantised SwiGLU output), ``swiglu_backward`` on the up
+    projection's output ``gu`` (recomputed from yq as ``_recompute_block``
+    does), then the up projection's ``backward_qmm`` (dout = d_gu with the
+    abs-max swiglu_backward recorded, inp = the quantised LN2 output).
+    Returns d_ln2, dw1, dw2, dh, gu, d_gu and the two stats pairs.
+    """
+    dh, dw2, dq, ds = backward_qmm(dout_bits, dout_amax, hq_codes, h_scale, w2_codes, w2_scale, dw2_old)
+    gu = fp8_gemm_scaled(yq_codes, y_scale, w1_codes, w1_scale)
+    d_gu, amax_dgu = swiglu_backward(dh, gu, H)
+    d_ln2, dw1, dguq, sdgu = backward_qmm(d_gu, amax_dgu, yq_codes, y_scale, w1_codes, w1_scale, dw1_old)
+    return {
+        "dh": dh, "dw2": dw2, "dout_q": dq, "stats_dout": np.array([dout_amax, ds], dtype=np.float32),
+        "gu": gu, "d_gu": d_gu, "d_gu_q": dguq,
+        "stats_dgu": np.array([amax_dgu, sdgu], dtype=np.float32), "d_ln2": d_ln2, "dw1": dw1,
     }
 
 

@@ -188,6 +188,39 @@ def silu_times(g_bits: int, u_bits: int) -> int:
     return round_bf16(Fraction(s) * u)
 
 
+def _dec(f: Fraction) -> Decimal:
+    return Decimal(f.numerator) / Decimal(f.denominator)
+
+
+def swiglu_grad(dh_bits: int, g_bits: int, u_bits: int) -> tuple[int, int]:
+    """(dg, du) of h = silu(g) * u, from the closed-form derivative, each rounded once."""
+    g, u, dh = _dec(bf16_value(g_bits)), bf16_value(u_bits), bf16_value(dh_bits)
+    sig = Decimal(1) / (Decimal(1) + (-g).exp())
+    dsilu = sig * (Decimal(1) + g * (Decimal(1) - sig))
+    return round_bf16(Fraction(dsilu) * u * dh), round_bf16(Fraction(g * sig) * dh)
+
+
+def silu_times_u_fd(g_bits: int, u_bits: int, dh_bits: int) -> int:
+    """dh * d/dg [silu(g) * u] by a central difference (60-digit decimals, step 1e-18), rounded once."""
+    g, u, dh = _dec(bf16_value(g_bits)), _dec(bf16_value(u_bits)), _dec(bf16_value(dh_bits))
+    eps = Decimal(10) ** -18
+
+    def f(z):
+        return z / (Decimal(1) + (-z).exp()) * u
+    return round_bf16(Fraction((f(g + eps) - f(g - eps)) / (2 * eps) * dh))
+
+
+def gemm_acc(a_codes, a_scale, w_codes, w_scale, old_bits):
+    """out[m][n] = bf16(old[m][n] + sa * sw * sum_k A[m][k] * W[n][k]), one rounding."""
+    sa, sw = Fraction(float(a_scale)), Fraction(float(w_scale))
+    out = []
+    for arow, orow_old in zip(a_codes, old_bits):
+        av = [e4m3_value(c) for c in arow]
+        out.append([round_bf16(bf16_value(o) + sum(x * e4m3_value(c) for x, c in zip(av, wrow)) * sa * sw)
+                    for wrow, o in zip(w_codes, orow_old)])
+    return out
+
+
 def gemv(x_bits, w_codes, row_scales):
     xv = [bf16_value(b) for b in x_bits]
     out = []

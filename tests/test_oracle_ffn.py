@@ -413,3 +413,83 @@ def test_qmm_identity_weight_closed_form():
     want = oracle.f64_to_bf16(oracle.e4m3_decode(codes) * float(scale) * 448.0 * float(np.float32(1 / 448.0))
                               + oracle.bf16_to_f64(bias)[None, :])
     np.testing.assert_array_equal(out, want)
+
+
+# ------------------------------------------------------------------ FFN backward (FP8)
+def test_swiglu_backward_matches_brute_force_and_layout():
+    H = 10
+    gu = _mixed_bf16((3, 2 * H), 121)
+    dh = _mixed_bf16((3, H), 122)
+    d, amax = oracle.swiglu_backward(dh, gu, H)
+    for i in range(3):
+        for j in range(H):
+            dg, du = brute.swiglu_grad(dh[i, j], gu[i, j], gu[i, H + j])
+            assert int(d[i, j]) == dg and int(d[i, H + j]) == du
+    assert amax == oracle.absmax(d)
+
+
+def test_swiglu_backward_derivative_by_finite_difference():
+    """The gate gradient is dh times the derivative of silu(g) * u, checked by a
+    central difference (not by the closed form)."""
+    H = 64
+    gu = random_bf16((4, 2 * H), seed=123, std=2.0)
+    dh = random_bf16((4, H), seed=124)
+    d, _ = oracle.swiglu_backward(dh, gu, H)
+    fd = np.array([[brute.silu_times_u_fd(gu[i, j], gu[i, H + j], dh[i, j]) for j in range(H)]
+                   for i in range(4)], dtype=np.uint16)
+    from gpu_util import bf16_ulp_diff
+    diff = bf16_ulp_diff(d[:, :H], fd)
+    assert diff.max() <= 1 and (diff == 0).mean() >= 0.98
+    # du is dh * silu(g), the forward's product with u replaced by dh
+    np.testing.assert_array_equal(d[:, H:], oracle.swiglu(np.concatenate([gu[:, :H], dh], axis=1), H)[0])
+
+
+def test_backward_qmm_matches_brute_force():
+    """dgrad over the output channels, wgrad over the tokens, and wgrad accumulation."""
+    N, IC, OC = 4, 16, 6
+    dout = _mixed_bf16((N, OC), 125)
+    amax = oracle.absmax(dout)
+    inq, ins = oracle.quantize_tensor(_mixed_bf16((N, IC), 126))
+    wq, ws = oracle.quantize_tensor(random_bf16((OC, IC), 127, std=0.02))
+    old = _mixed_bf16((OC, IC), 128)
+    dinp, dw, dq, ds = oracle.backward_qmm(dout, amax, inq, ins, wq, ws)
+    _, dwa, _, _ = oracle.backward_qmm(dout, amax, inq, ins, wq, ws, old)
+    bq, bs = brute.quantize(list(dout.ravel()), float(amax))
+    rows = [bq[i * OC:(i + 1) * OC] for i in range(N)]
+    assert dq.tolist() == rows and Fraction(float(ds)) == bs
+    wt = [list(c) for c in zip(*wq.tolist())]                 # W^T: [IC][OC]
+    assert dinp.tolist() == brute.gemm(rows, float(bs), wt, ws)
+    dqt = [list(c) for c in zip(*rows)]                        # dout_q^T: [OC][N]
+    int_ = [list(c) for c in zip(*inq.tolist())]               # inp^T: [IC][N]
+    assert dw.tolist() == brute.gemm(dqt, float(bs), int_, ins)
+    assert dwa.tolist() == brute.gemm_acc(dqt, float(bs), int_, ins, old.tolist())
+
+
+def test_ffn_backward_tiny_brute_force_chain():
+    N, C, H = 3, 8, 4
+    dout = _mixed_bf16((N, C), 131)
+    yq, sy = oracle.quantize_tensor(_mixed_bf16((N, C), 132))
+    hq, sh = oracle.quantize_tensor(_mixed_bf16((N, H), 133))
+    w1q, w1s = oracle.quantize_tensor(random_bf16((2 * H, C), 134, std=0.02))
+    w2q, w2s = oracle.quantize_tensor(random_bf16((C, H), 135, std=0.02))
+    amax = oracle.absmax(dout)
+    o = oracle.ffn_backward(dout, amax, yq, sy, hq, sh, w1q, w1s, w2q, w2s, H)
+    T = lambda m: [list(c) for c in zip(*m)]
+    dq, ds = brute.quantize(list(dout.ravel()), float(amax))
+    dq = [dq[i * C:(i + 1) * C] for i in range(N)]
+    dh = brute.gemm(dq, float(ds), T(w2q.tolist()), w2s)
+    assert o["dh"].tolist() == dh
+    assert o["dw2"].tolist() == brute.gemm(T(dq), float(ds), T(hq.tolist()), sh)
+    gu = brute.gemm(yq.tolist(), sy, w1q.tolist(), w1s)
+    assert o["gu"].tolist() == gu
+    dgu = [[0] * (2 * H) for _ in range(N)]
+    for i in range(N):
+        for j in range(H):
+            dgu[i][j], dgu[i][H + j] = brute.swiglu_grad(dh[i][j], gu[i][j], gu[i][H + j])
+    assert o["d_gu"].tolist() == dgu
+    amax_g = max(abs(brute.bf16_value(b)) for row in dgu for b in row)
+    assert Fraction(float(o["stats_dgu"][0])) == amax_g
+    gq, gs = brute.quantize([b for row in dgu for b in row], float(amax_g))
+    gq = [gq[i * 2 * H:(i + 1) * 2 * H] for i in range(N)]
+    assert o["d_ln2"].tolist() == brute.gemm(gq, float(gs), T(w1q.tolist()), w1s)
+    assert o["dw1"].tolist() == brute.gemm(T(gq), float(gs), T(yq.tolist()), sy)
