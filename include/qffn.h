@@ -223,6 +223,73 @@ qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd
                                   int64_t B, int64_t T, int64_t C, int64_t H, void* workspace,
                                   size_t workspace_bytes, qffn_stream_t stream);
 
+/* ---- FP8 backward of the FFN -----------------------------------------------
+ * [llmq-model] _backward_block (FFN half) and the FP8 branch of backward_qmm.
+ * Gradients are bf16; their FP8 copies are E4M3 quantised with a recorded
+ * abs-max, exactly as activations are (qffn_quantize). */
+
+/* E4M3 transpose: out[cols, rows] = in[rows, cols]^T (backward_qmm's
+ * transpose of the weight and of the quantised operands).  rows and cols are
+ * multiples of 16; rows < 64 * 65535. */
+qffn_status qffn_transpose_e4m3(uint8_t* out, const uint8_t* in, int64_t rows, int64_t cols,
+                                qffn_stream_t stream);
+
+/* [llmq-model] swiglu_backward(DMlpUp.Value, DSwiGLU, MlpUp,
+ * DMlpUp.Quant.abs_max(), B, T, D).  With g, u the bf16 gate / up halves of
+ * gate_up [N, 2H] and dh [N, H] the gradient of h = silu(g) * u:
+ *   d_gate_up[:, j]     = bf16(dh * u * s * (1 + g * (1 - s))),  s = sigmoid(g)
+ *   d_gate_up[:, H + j] = bf16(dh * silu(g))
+ *   stats[0] = max |d_gate_up|   (zeroed first)
+ * fp32 arithmetic, one rounding per output.  N >= 0, H % 8 == 0. */
+qffn_status qffn_swiglu_backward(uint16_t* d_gate_up, float* stats, const uint16_t* dh,
+                                 const uint16_t* gate_up, int64_t N, int64_t H,
+                                 qffn_stream_t stream);
+
+/* [llmq-model] backward_qmm, FP8 weights, for one projection out = inp @ W^T
+ * with dout [N, OC] bf16, the forward's quantised input inp_q [N, IC] E4M3 with
+ * inp_scale[1], W [OC, IC] E4M3 with w_scale[1]:
+ *   dq = e4m3(dout * 448 / stats_dout[0]);  stats_dout[1] = scale
+ *   dinp[N, IC] = bf16(stats_dout[1] * w_scale * sum_oc dq[n, oc] * W[oc, ic])
+ *   dw[OC, IC]  = bf16(stats_dout[1] * inp_scale * sum_n dq[n, oc] * inp_q[n, ic]
+ *                      (+ dw[OC, IC] when accumulate != 0))
+ * stats_dout[0] is the recorded abs-max of dout (an input).  dinp may be NULL
+ * (weight gradient only).  As on the page, the weight and both operands of
+ * the weight gradient are transposed into the workspace so that each matmul
+ * is K-contiguous.  workspace: >= qffn_backward_qmm_workspace_size() bytes,
+ * 256-byte aligned.  N % 16 == 0, IC % 32 == 0, OC % 32 == 0 (all >= 32
+ * except N >= 0), IC, OC <= 2^20. */
+size_t qffn_backward_qmm_workspace_size(int64_t N, int64_t IC, int64_t OC);
+qffn_status qffn_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout,
+                              const uint16_t* dout, const uint8_t* inp_q, const float* inp_scale,
+                              const uint8_t* w, const float* w_scale, int64_t N, int64_t IC,
+                              int64_t OC, int accumulate, void* workspace, size_t workspace_bytes,
+                              qffn_stream_t stream);
+
+/* The FFN half of _backward_block after the norm, for the block output
+ * gradient dout [N, C] (bf16, stats_dout[0] = its recorded abs-max):
+ *   1. backward_qmm of the down projection (inp = hq [N, H] of the forward,
+ *      W2 [C, H]) -> dh [N, H], dw2 [C, H];
+ *   2. the up projection's output gate_up [N, 2H] recomputed from yq and W1
+ *      (forward_qmm of _recompute_block);
+ *   3. swiglu_backward -> d_gate_up [N, 2H], stats_dgu[0] = its abs-max;
+ *   4. backward_qmm of the up projection (inp = yq [N, C], W1 [2H, C])
+ *      -> d_ln2 [N, C], dw1 [2H, C].
+ * stats_dout[1] and stats_dgu[1] receive the two gradient scales.  With
+ * accumulate != 0 the weight gradients add to dw1 and dw2.  workspace: >=
+ * qffn_ffn_backward_workspace_size() bytes, 256-byte aligned; after the call
+ * it holds dh, gate_up and d_gate_up (bf16) at the offsets that
+ * qffn_ffn_backward_workspace_offsets() returns.  N % 16 == 0,
+ * C % 32 == 0, H % 128 == 0, C, H >= 128. */
+size_t qffn_ffn_backward_workspace_size(int64_t N, int64_t C, int64_t H);
+qffn_status qffn_ffn_backward_workspace_offsets(int64_t N, int64_t C, int64_t H,
+                                                size_t offsets[3] /* dh, gate_up, d_gate_up */);
+qffn_status qffn_ffn_backward(uint16_t* d_ln2, uint16_t* dw1, uint16_t* dw2, float* stats_dout,
+                              float* stats_dgu, const uint16_t* dout, const uint8_t* yq,
+                              const float* y_scale, const uint8_t* hq, const float* h_scale,
+                              const uint8_t* w1, const float* w1_scale, const uint8_t* w2,
+                              const float* w2_scale, int64_t N, int64_t C, int64_t H, int accumulate,
+                              void* workspace, size_t workspace_bytes, qffn_stream_t stream);
+
 /* ---- Step A6: dual row-scaled FP8 GEMV ------------------------------------
  * [metrale] w8a16_gemv_dual: one pass over x for two weight matrices.
  *   g[r] = bf16(s_gate[r] * sum_k Wg[r,k] * x[k]),  u likewise with Wu, s_up.

@@ -164,3 +164,22 @@ def test_qmm_checks(lib):
     assert f(A, A, A, A, NULL, A, A, 4, 48, 16, None) == 2      # N % 32
     assert f(A, A, A, A, NULL, A, A, 4, 32, 24, None) == 2      # K % 16
     assert f(A, A, A, A, MIS, A, A, 4, 32, 16, None) == 3       # bias misaligned
+
+
+def test_backward_checks(lib):
+    assert lib.qffn_backward_qmm_workspace_size(64, 256, 128) > 0
+    assert lib.qffn_backward_qmm_workspace_size(60, 256, 128) == 0          # N % 16
+    assert lib.qffn_ffn_backward_workspace_size(64, 256, 768) > 0
+    assert lib.qffn_ffn_backward_workspace_size(64, 256, 200) == 0          # H % 128
+    off = lib.qffn_ffn_backward_workspace_offsets(64, 256, 768)
+    assert off[0] == 0 and off[1] >= 64 * 768 * 2 and off[2] >= off[1] + 64 * 1536 * 2
+    assert all(o % 256 == 0 for o in off)
+    assert _call(lib, "qffn_transpose_e4m3", A, A, 24, 16, None) == 2
+    assert _call(lib, "qffn_transpose_e4m3", MIS, A, 16, 16, None) == 3
+    assert _call(lib, "qffn_swiglu_backward", A, A, A, A, 4, 12, None) == 2
+    ws = lib.qffn_backward_qmm_workspace_size(64, 256, 128)
+    f = lambda *a: _call(lib, "qffn_backward_qmm", *a)
+    assert f(A, NULL, A, A, A, A, A, A, 64, 256, 128, 0, A, ws, None) == 1   # dw required
+    assert f(A, A, A, A, A, A, A, A, 64, 256, 128, 0, A, ws - 1, None) == 1
+    assert f(A, A, A, A, A, A, A, A, 64, 250, 128, 0, A, ws, None) == 2
+    assert f(A, A, A, A, A, A, A, A, 64, 256, 128, 0, A + 16, ws, None) == 3

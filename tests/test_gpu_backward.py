@@ -1,0 +1,215 @@
+"""GPU parity of the FP8 FFN backward (transpose, swiglu_backward, backward_qmm and the
+chain qffn_ffn_backward) through the C ABI, against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ffn_inputs import random_bf16, random_codes
+from gpu_util import (assert_out_close, bf, bf16_ulp_diff, check_dot_outputs, dev, empty_bf16,
+                      empty_u8, host, sync)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def q():
+    import transformer_ffn_block_gb300 as q
+    return q
+
+
+def _mixed(shape, seed, spread=1):
+    rng = np.random.default_rng(seed)
+    return oracle.f64_to_bf16(rng.standard_normal(shape) * 10.0 ** rng.integers(-spread, spread + 1, shape))
+
+
+def _absdot(a_codes, sa, b_codes, sb):
+    """scale * sum |terms| of out = A . B^T (the fp32 accumulation bound's magnitude)."""
+    return (np.abs(oracle.e4m3_decode(a_codes)) @ np.abs(oracle.e4m3_decode(b_codes)).T) * float(sa) * float(sb)
+
+
+@pytest.mark.parametrize("R,C", [(16, 16), (48, 80), (64, 128), (1040, 336), (4096, 14336)])
+def test_transpose_e4m3(q, R, C):
+    a = random_codes((R, C), seed=R + C)
+    out = empty_u8(C, R)
+    q.qffn_transpose_e4m3(out, dev(a), R, C)
+    sync()
+    np.testing.assert_array_equal(host(out), a.T)
+
+
+def _check_swiglu_grad(got, want):
+    """<= 1 bf16 ulp, except where silu'(g) is near its root (g ~ -1.28): there the
+    fp32 value of 1 + g (1 - sigmoid(g)) cancels, so a few tiny outputs may differ more."""
+    d = bf16_ulp_diff(got, want)
+    w = np.abs(oracle.bf16_to_f64(want))
+    bad = d > 1
+    assert bad.mean() <= 1e-3
+    if bad.any():
+        assert np.all(w[bad] <= 1e-2 * w.max())
+
+
+@pytest.mark.parametrize("N,H", [(1, 8), (64, 768), (333, 1024), (16, 14336)])
+def test_swiglu_backward(q, N, H):
+    gu = _mixed((N, 2 * H), N + H)
+    dh = _mixed((N, H), N * 3 + H)
+    d = empty_bf16(N, 2 * H)
+    stats = torch.full((2,), 5.0, dtype=torch.float32, device="cuda")
+    q.qffn_swiglu_backward(d, stats, dev(dh), dev(gu), N, H)
+    sync()
+    got = bf(d)
+    want, _ = oracle.swiglu_backward(dh, gu, H)
+    _check_swiglu_grad(got, want)
+    st = host(stats)
+    assert st[0] == np.float32(np.max(np.abs(oracle.bf16_to_f64(got))))     # its own abs-max, exactly
+    assert st[1] == 5.0
+
+
+@pytest.mark.parametrize("N,IC,OC,acc", [(48, 96, 64, False), (64, 256, 128, True), (256, 512, 384, False),
+                                         (512, 1024, 2048, True)])
+def test_backward_qmm(q, N, IC, OC, acc):
+    dout = random_bf16((N, OC), seed=N + OC, std=1e-3)
+    inq, ins = oracle.quantize_tensor(random_bf16((N, IC), seed=N + IC))
+    wq, ws = oracle.quantize_tensor(random_bf16((OC, IC), seed=OC + IC, std=0.02))
+    old = random_bf16((OC, IC), seed=7, std=1e-2)
+    amax = oracle.absmax(dout)
+    stats = torch.tensor([amax, -1.0], dtype=torch.float32, device="cuda")
+    sc = torch.tensor([ins, ws], dtype=torch.float32, device="cuda")
+    dinp = empty_bf16(N, IC)
+    dw = dev(old) if acc else empty_bf16(OC, IC)
+    wsb = torch.empty(q.qffn_backward_qmm_workspace_size(N, IC, OC), dtype=torch.uint8, device="cuda")
+    q.qffn_backward_qmm(dinp, dw, stats, dev(dout), dev(inq), sc[0:1], dev(wq), sc[1:2], N, IC, OC, acc, wsb)
+    q.qffn_check_status()
+    sync()
+    rd, rw, rq, rs = oracle.backward_qmm(dout, amax, inq, ins, wq, ws, old if acc else None)
+    assert host(stats)[1] == rs
+    np.testing.assert_array_equal(host(wsb[:N * OC]).reshape(N, OC), rq)       # dout codes
+    check_dot_outputs(bf(dinp), rd, _absdot(rq, rs, wq.T, ws), OC, max_mismatch=2e-3)
+    check_dot_outputs(bf(dw), rw, _absdot(rq.T, rs, inq.T, ins), N, max_mismatch=2e-3)
+
+
+def _ffn_backward_dev(q, dout, amax, yq, sy, hq, sh, w1q, w1s, w2q, w2s, N, C, H, acc=False,
+                     dw_init=None):
+    """Runs qffn_ffn_backward; returns its outputs and workspace intermediates as
+    device tensors (bf16 bits as int16) plus the four stats words."""
+    st = torch.tensor([amax, -1.0, -1.0, -1.0], dtype=torch.float32, device="cuda")
+    sc = torch.tensor([sy, sh, w1s, w2s], dtype=torch.float32, device="cuda")
+    d_ln2 = empty_bf16(N, C)
+    dw1 = dev(dw_init[0]) if dw_init else empty_bf16(2 * H, C)
+    dw2 = dev(dw_init[1]) if dw_init else empty_bf16(C, H)
+    ws = torch.empty(q.qffn_ffn_backward_workspace_size(N, C, H), dtype=torch.uint8, device="cuda")
+    q.qffn_ffn_backward(d_ln2, dw1, dw2, st[0:2], st[2:4], dev(dout), dev(yq), sc[0:1], dev(hq), sc[1:2],
+                        dev(w1q), sc[2:3], dev(w2q), sc[3:4], N, C, H, acc, ws)
+    q.qffn_check_status()
+    sync()
+    off = q.qffn_ffn_backward_workspace_offsets(N, C, H)
+    return dict(d_ln2=d_ln2, dw1=dw1, dw2=dw2, st=host(st),
+                dh=ws[off[0]:off[0] + N * H * 2].view(torch.int16).view(N, H),
+                gu=ws[off[1]:off[1] + N * 2 * H * 2].view(torch.int16).view(N, 2 * H),
+                dgu=ws[off[2]:off[2] + N * 2 * H * 2].view(torch.int16).view(N, 2 * H))
+
+
+def _ffn_backward_gpu(*a, **k):
+    g = _ffn_backward_dev(*a, **k)
+    return {key: (v if key == "st" else bf(v)) for key, v in g.items()}
+
+
+def _backward_inputs(N, C, H, seed):
+    dout = random_bf16((N, C), seed=seed, std=1e-3)
+    yq, sy = oracle.quantize_tensor(random_bf16((N, C), seed=seed + 1))
+    h = oracle.swiglu(oracle.f64_to_bf16(np.random.default_rng(seed + 2).standard_normal((N, 2 * H))), H)[0]
+    hq, sh = oracle.quantize_tensor(h)
+    w1q, w1s = oracle.quantize_tensor(random_bf16((2 * H, C), seed=seed + 3, std=0.02))
+    w2q, w2s = oracle.quantize_tensor(random_bf16((C, H), seed=seed + 4, std=0.02))
+    return dout, yq, sy, hq, sh, w1q, w1s, w2q, w2s
+
+
+@pytest.mark.parametrize("N,C,H", [(64, 256, 768), (512, 1024, 2048)])
+def test_ffn_backward_stagewise_and_end_to_end(q, N, C, H):
+    dout, yq, sy, hq, sh, w1q, w1s, w2q, w2s = _backward_inputs(N, C, H, N + C + H)
+    amax = oracle.absmax(dout)
+    g = _ffn_backward_gpu(q, dout, amax, yq, sy, hq, sh, w1q, w1s, w2q, w2s, N, C, H)
+    st = g["st"]
+    # down projection, fed the same dout
+    rdh, rdw2, rq, rs = oracle.backward_qmm(dout, amax, hq, sh, w2q, w2s)
+    assert st[1] == rs
+    check_dot_outputs(g["dh"], rdh, _absdot(rq, rs, w2q.T, w2s), C, 2e-3)
+    check_dot_outputs(g["dw2"], rdw2, _absdot(rq.T, rs, hq.T, sh), N, 2e-3)
+    # recomputed up-projection output
+    check_dot_outputs(g["gu"], oracle.fp8_gemm_scaled(yq, sy, w1q, w1s), _absdot(yq, sy, w1q, w1s), C, 2e-3)
+    # swiglu_backward on the GPU's own dh and gate|up
+    rdgu, _ = oracle.swiglu_backward(g["dh"], g["gu"], H)
+    _check_swiglu_grad(g["dgu"], rdgu)
+    assert st[2] == np.float32(np.max(np.abs(oracle.bf16_to_f64(g["dgu"]))))
+    # up projection, fed the GPU's own d_gate_up and its abs-max
+    rdl, rdw1, rq1, rs1 = oracle.backward_qmm(g["dgu"], st[2], yq, sy, w1q, w1s)
+    assert st[3] == rs1
+    check_dot_outputs(g["d_ln2"], rdl, _absdot(rq1, rs1, w1q.T, w1s), 2 * H, 2e-3)
+    check_dot_outputs(g["dw1"], rdw1, _absdot(rq1.T, rs1, yq.T, sy), N, 2e-3)
+    # end to end against the oracle chain: the block-output tolerance
+    ref = oracle.ffn_backward(dout, amax, yq, sy, hq, sh, w1q, w1s, w2q, w2s, H)
+    for k in ("d_ln2", "dw1", "dw2"):
+        assert_out_close(g[k], ref[k])
+
+
+def test_ffn_backward_accumulates_weight_gradients(q):
+    N, C, H = 64, 256, 256
+    args = _backward_inputs(N, C, H, 17)
+    dout = args[0]
+    amax = oracle.absmax(dout)
+    old1, old2 = random_bf16((2 * H, C), seed=41, std=1e-2), random_bf16((C, H), seed=42, std=1e-2)
+    g0 = _ffn_backward_gpu(q, dout, amax, *args[1:], N, C, H)
+    g1 = _ffn_backward_gpu(q, dout, amax, *args[1:], N, C, H, acc=True, dw_init=(old1, old2))
+    np.testing.assert_array_equal(g1["d_ln2"], g0["d_ln2"])              # dinp is not accumulated
+    yq, sy, hq, sh, w1q, w1s, w2q, w2s = args[1:]
+    _, rdw2, rq, rs = oracle.backward_qmm(dout, amax, hq, sh, w2q, w2s, old2)
+    check_dot_outputs(g1["dw2"], rdw2, _absdot(rq.T, rs, hq.T, sh), N, 2e-3)
+    _, rdw1, rq1, rs1 = oracle.backward_qmm(g1["dgu"], g1["st"][2], yq, sy, w1q, w1s, old1)
+    check_dot_outputs(g1["dw1"], rdw1, _absdot(rq1.T, rs1, yq.T, sy), N, 2e-3)
+
+
+def test_ffn_backward_8b_shape_sampled(q):
+    """The Llama-3-8B FFN backward (N=16384, C=4096, H=14336) in the configuration the
+    benchmark times, checked on sampled outputs stage by stage: each stage is fed the
+    GPU's own upstream tensors, and weight-gradient entries are sampled dot products
+    over all tokens.  The forward's quantised SwiGLU output is a random code tensor."""
+    N, C, H = 16384, 4096, 14336
+    dout = random_bf16((N, C), seed=99, std=1e-3)
+    yq, sy = oracle.quantize_tensor(random_bf16((N, C), seed=100))
+    hq, sh = random_codes((N, H), seed=101), np.float32(1 / 448.0)
+    w1q, w1s = oracle.quantize_tensor(random_bf16((2 * H, C), seed=102, std=0.02))
+    w2q, w2s = oracle.quantize_tensor(random_bf16((C, H), seed=103, std=0.02))
+    amax = oracle.absmax(dout)
+    g = _ffn_backward_dev(q, dout, amax, yq, sy, hq, sh, w1q, w1s, w2q, w2s, N, C, H)
+    st = g["st"]
+    rng = np.random.default_rng(3)
+    rows = np.sort(rng.choice(N, 12, replace=False))
+    ridx = torch.from_numpy(rows).cuda()
+    dq, ds = oracle.quantize_with_abs_max(dout, amax)
+    assert st[1] == ds
+    dh_r, gu_r, dgu_r = (bf(g[k].index_select(0, ridx)) for k in ("dh", "gu", "dgu"))
+    rdh = oracle.fp8_gemm_scaled(dq[rows], ds, np.ascontiguousarray(w2q.T), w2s)
+    check_dot_outputs(dh_r, rdh, _absdot(dq[rows], ds, w2q.T, w2s), C, 2e-3)
+    rgu = oracle.fp8_gemm_scaled(yq[rows], sy, w1q, w1s)
+    check_dot_outputs(gu_r, rgu, _absdot(yq[rows], sy, w1q, w1s), C, 2e-3)
+    _check_swiglu_grad(dgu_r, oracle.swiglu_backward(dh_r, gu_r, H)[0])
+    # the recorded abs-max of d_gate_up is the max of the GPU's own tensor
+    assert st[2] == float(g["dgu"].view(torch.bfloat16).abs().max().float())
+    gq_r, gs = oracle.quantize_with_abs_max(dgu_r, st[2])
+    assert st[3] == gs
+    rdl = oracle.fp8_gemm_scaled(gq_r, gs, np.ascontiguousarray(w1q.T), w1s)
+    # a 28672-term reduction of gradient products cancels heavily (|sum| ~ sum|terms| /
+    # sqrt(K)), so fp32 accumulation flips the bf16 rounding of more outputs than in the
+    # forward; every output still meets the error bound, and at most 1% may differ
+    check_dot_outputs(bf(g["d_ln2"].index_select(0, ridx)), rdl, _absdot(gq_r, gs, w1q.T, w1s), 2 * H, 1e-2)
+    # weight gradients: 16 x 16 sampled entries each, dot products over all N tokens
+    oi = np.sort(rng.choice(C, 16, replace=False))
+    ii = np.sort(rng.choice(H, 16, replace=False))
+    want = oracle.fp8_gemm_scaled(np.ascontiguousarray(dq[:, oi].T), ds, np.ascontiguousarray(hq[:, ii].T), sh)
+    got = bf(g["dw2"])[np.ix_(oi, ii)]
+    check_dot_outputs(got, want, _absdot(dq[:, oi].T, ds, hq[:, ii].T, sh), N, 2e-2)
+    oi = np.sort(rng.choice(2 * H, 16, replace=False))
+    ii = np.sort(rng.choice(C, 16, replace=False))
+    gq_c, _ = oracle.quantize_with_abs_max(bf(g["dgu"].index_select(1, torch.from_numpy(oi).cuda())), st[2])
+    want = oracle.fp8_gemm_scaled(np.ascontiguousarray(gq_c.T), gs, np.ascontiguousarray(yq[:, ii].T), sy)
+    got = bf(g["dw1"])[np.ix_(oi, ii)]
+    check_dot_outputs(got, want, _absdot(gq_c.T, gs, yq[:, ii].T, sy), N, 2e-2)

@@ -22,7 +22,9 @@ __all__ = [
     "qffn_fp8_gemm_scaled", "qffn_qmm", "qffn_gate_up_swiglu", "qffn_swiglu_quant",
     "qffn_swiglu_forward_quant", "qffn_gate_up_swiglu_quant",
     "qffn_forward_workspace_size", "qffn_forward_workspace_offsets", "qffn_forward",
-    "qffn_forward_recompute",
+    "qffn_forward_recompute", "qffn_transpose_e4m3", "qffn_swiglu_backward",
+    "qffn_backward_qmm_workspace_size", "qffn_backward_qmm", "qffn_ffn_backward_workspace_size",
+    "qffn_ffn_backward_workspace_offsets", "qffn_ffn_backward",
     "qffn_gemv_dual", "qffn_gemv", "qffn_gemv_silu_input", "qffn_silu_mul", "qffn_decode_workspace_size",
     "qffn_decode_forward", "qffn_decode_forward_noalloc",
 ]
@@ -63,6 +65,14 @@ _SIGS = {
                       _I64, _I64, _I64, _I64, _P, _SZ, _P], _S),
     "qffn_forward_recompute": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _P, _P, _P, _P,
                                 _I64, _I64, _I64, _I64, _P, _SZ, _P], _S),
+    "qffn_transpose_e4m3": ([_P, _P, _I64, _I64, _P], _S),
+    "qffn_swiglu_backward": ([_P, _P, _P, _P, _I64, _I64, _P], _S),
+    "qffn_backward_qmm_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "qffn_backward_qmm": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _S, _P, _SZ, _P], _S),
+    "qffn_ffn_backward_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "qffn_ffn_backward_workspace_offsets": ([_I64, _I64, _I64, ctypes.POINTER(_SZ)], _S),
+    "qffn_ffn_backward": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                           _I64, _I64, _I64, _S, _P, _SZ, _P], _S),
     "qffn_gemv_dual": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], _S),
     "qffn_gemv": ([_P, _P, _P, _P, _I64, _I64, _P], _S),
     "qffn_gemv_silu_input": ([_P, _P, _P, _P, _P, _I64, _I64, _P], _S),
@@ -201,6 +211,53 @@ def qffn_forward_recompute(res_out, out, rstd, stats_y, stats_h, res_in, x, gain
         _ptr(res_out), _ptr(out), _ptr(rstd), _ptr(stats_y), _ptr(stats_h), _ptr(res_in),
         _ptr(x), _ptr(gain), float(eps), _ptr(w1), _ptr(w1_scale), _ptr(w2), _ptr(w2_scale),
         int(B), int(T), int(C), int(H), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
+def qffn_transpose_e4m3(out, inp, rows, cols, stream=None):
+    _check("qffn_transpose_e4m3", lib.qffn_transpose_e4m3(
+        _ptr(out), _ptr(inp), int(rows), int(cols), _stream(stream)))
+
+
+def qffn_swiglu_backward(d_gate_up, stats, dh, gate_up, N, H, stream=None):
+    _check("qffn_swiglu_backward", lib.qffn_swiglu_backward(
+        _ptr(d_gate_up), _ptr(stats), _ptr(dh), _ptr(gate_up), int(N), int(H), _stream(stream)))
+
+
+def qffn_backward_qmm_workspace_size(N, IC, OC) -> int:
+    return int(lib.qffn_backward_qmm_workspace_size(int(N), int(IC), int(OC)))
+
+
+def qffn_backward_qmm(dinp, dw, stats_dout, dout, inp_q, inp_scale, w, w_scale, N, IC, OC,
+                      accumulate, workspace, workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("qffn_backward_qmm", lib.qffn_backward_qmm(
+        _ptr(dinp), _ptr(dw), _ptr(stats_dout), _ptr(dout), _ptr(inp_q), _ptr(inp_scale), _ptr(w),
+        _ptr(w_scale), int(N), int(IC), int(OC), int(bool(accumulate)), _ptr(workspace),
+        int(workspace_bytes), _stream(stream)))
+
+
+def qffn_ffn_backward_workspace_size(N, C, H) -> int:
+    return int(lib.qffn_ffn_backward_workspace_size(int(N), int(C), int(H)))
+
+
+def qffn_ffn_backward_workspace_offsets(N, C, H) -> list[int]:
+    off = (_SZ * 3)()
+    _check("qffn_ffn_backward_workspace_offsets",
+           lib.qffn_ffn_backward_workspace_offsets(int(N), int(C), int(H), off))
+    return [int(v) for v in off]
+
+
+def qffn_ffn_backward(d_ln2, dw1, dw2, stats_dout, stats_dgu, dout, yq, y_scale, hq, h_scale, w1,
+                      w1_scale, w2, w2_scale, N, C, H, accumulate, workspace, workspace_bytes=None,
+                      stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("qffn_ffn_backward", lib.qffn_ffn_backward(
+        _ptr(d_ln2), _ptr(dw1), _ptr(dw2), _ptr(stats_dout), _ptr(stats_dgu), _ptr(dout), _ptr(yq),
+        _ptr(y_scale), _ptr(hq), _ptr(h_scale), _ptr(w1), _ptr(w1_scale), _ptr(w2), _ptr(w2_scale),
+        int(N), int(C), int(H), int(bool(accumulate)), _ptr(workspace), int(workspace_bytes),
+        _stream(stream)))
 
 
 def qffn_gemv_dual(g, u, x, w_gate, s_gate, w_up, s_up, H, C, stream=None):

@@ -1,6 +1,6 @@
 """Build libqffn.so in-tree with nvcc for sm_103a.
 
-The four translation units are compiled in parallel into ``_build/`` and
+The translation units are compiled in parallel into ``_build/`` and
 linked into ``transformer_ffn_block_gb300/libqffn.so`` (CUDA runtime linked
 statically; the driver's tensor-map encoder is fetched at run time).
 """
@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqffn.so")
 
-SOURCES = ["api.cu", "elementwise.cu", "gemm_fp8.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "elementwise.cu", "gemm_fp8.cu", "decode.cu", "decode_noalloc.cu", "backward.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "launch.h", "pipeline.cuh")] + [os.path.join(INCLUDE, "qffn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3",

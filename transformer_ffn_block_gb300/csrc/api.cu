@@ -44,6 +44,66 @@ void forward_offsets(int64_t N, int64_t C, int64_t H, size_t off[5]) {
   off[4] = round_up(off[3] + size_t(N) * size_t(H), 256);
 }
 
+// backward_qmm workspace: dout_q [N,OC] | dout_q^T [OC,N] | inp_q^T [IC,N] | W^T [IC,OC],
+// E4M3, each 256-byte aligned
+void bqmm_offsets(int64_t N, int64_t IC, int64_t OC, size_t off[5]) {
+  off[0] = 0;
+  off[1] = round_up(off[0] + size_t(N) * size_t(OC), 256);
+  off[2] = round_up(off[1] + size_t(OC) * size_t(N), 256);
+  off[3] = round_up(off[2] + size_t(IC) * size_t(N), 256);
+  off[4] = round_up(off[3] + size_t(IC) * size_t(OC), 256);
+}
+
+// FFN backward workspace: dh [N,H] bf16 | gu [N,2H] bf16 | d_gu [N,2H] bf16 |
+// the larger of the two backward_qmm workspaces
+void ffn_bwd_offsets(int64_t N, int64_t C, int64_t H, size_t off[5]) {
+  size_t down[5], up[5];
+  bqmm_offsets(N, H, C, down);
+  bqmm_offsets(N, C, 2 * H, up);
+  off[0] = 0;
+  off[1] = round_up(size_t(N) * size_t(H) * 2, 256);
+  off[2] = round_up(off[1] + size_t(N) * size_t(2 * H) * 2, 256);
+  off[3] = round_up(off[2] + size_t(N) * size_t(2 * H) * 2, 256);
+  off[4] = off[3] + (down[4] > up[4] ? down[4] : up[4]);
+}
+
+qffn_status check_bqmm_shape(int64_t N, int64_t IC, int64_t OC) {
+  QFFN_REQUIRE(N >= 0 && IC >= 0 && OC >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(N % 16 == 0 && N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(IC % 32 == 0 && IC >= 32 && IC <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(OC % 32 == 0 && OC >= 32 && OC <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  return QFFN_OK;
+}
+
+// The FP8 branch of backward_qmm on pointers already checked; ws holds bqmm_offsets.
+cudaError_t run_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout, const uint16_t* dout,
+                             const uint8_t* inp_q, const float* inp_scale, const uint8_t* w,
+                             const float* w_scale, int64_t N, int64_t IC, int64_t OC,
+                             bool accumulate, uint8_t* ws, cudaStream_t s) {
+  size_t off[5];
+  bqmm_offsets(N, IC, OC, off);
+  uint8_t* dq = ws + off[0];
+  uint8_t* dqt = ws + off[1];
+  uint8_t* inpt = ws + off[2];
+  uint8_t* wt = ws + off[3];
+  cudaError_t e;
+  // quantize_with_abs_max(dout.Quant, scale, dout.Value, dout.Quant.abs_max())
+  if ((e = qffn::launch_quantize(dq, stats_dout, dout, N * OC, s)) != cudaSuccess) return e;
+  if (dinp != nullptr) {
+    // dinp[N,IC] = dout_q[N,OC] . (W^T)[IC,OC]^T, scales W.scale * dout.scale
+    if ((e = qffn::launch_transpose_u8(wt, w, OC, IC, s)) != cudaSuccess) return e;
+    if ((e = qffn::launch_gemm_bf16(dinp, dq, stats_dout + 1, wt, w_scale, N, IC, OC, s)) != cudaSuccess)
+      return e;
+  }
+  // no tokens: the weight gradient is a sum over nothing (0, or unchanged when accumulating)
+  if (N == 0) return accumulate ? cudaSuccess : cudaMemsetAsync(dw, 0, size_t(OC) * size_t(IC) * 2, s);
+  // dW[OC,IC] (+)= (dout_q^T)[OC,N] . (inp_q^T)[IC,N]^T, scales inp.scale * dout.scale
+  if ((e = qffn::launch_transpose_u8(dqt, dq, N, OC, s)) != cudaSuccess) return e;
+  if ((e = qffn::launch_transpose_u8(inpt, inp_q, N, IC, s)) != cudaSuccess) return e;
+  return qffn::launch_gemm_bf16(dw, dqt, stats_dout + 1, inpt, inp_scale, OC, IC, N, s, nullptr,
+                                accumulate);
+}
+
 // decode workspace: g [H] bf16 | u [H] bf16, each 256-byte aligned
 void decode_offsets(int64_t H, size_t off[2]) {
   off[0] = round_up(size_t(H) * 2, 256);   // u
@@ -299,6 +359,107 @@ qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd
   QFFN_CUDA(qffn::launch_gemm_swiglu_quant(hq, stats_h, yq, stats_y + 1, w1, w1_scale, N, H, C, stream));
   // A5: out
   return from_cuda(qffn::launch_gemm_bf16(out, hq, stats_h + 1, w2, w2_scale, N, C, H, stream));
+}
+
+qffn_status qffn_transpose_e4m3(uint8_t* out, const uint8_t* in, int64_t rows, int64_t cols,
+                                qffn_stream_t stream) {
+  QFFN_PTR(out); QFFN_PTR(in);
+  QFFN_REQUIRE(rows >= 0 && cols >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(rows % 16 == 0 && cols % 16 == 0 && rows <= kMaxRows && cols <= kMaxRows,
+               QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(rows / 64 < 65535, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(out); QFFN_ALIGNED(in);
+  return from_cuda(qffn::launch_transpose_u8(out, in, rows, cols, stream));
+}
+
+qffn_status qffn_swiglu_backward(uint16_t* d_gate_up, float* stats, const uint16_t* dh,
+                                 const uint16_t* gate_up, int64_t N, int64_t H,
+                                 qffn_stream_t stream) {
+  QFFN_PTR(d_gate_up); QFFN_PTR(stats); QFFN_PTR(dh); QFFN_PTR(gate_up);
+  QFFN_REQUIRE(N >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(H % 8 == 0 && H >= 8 && H <= kMaxDim && N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(d_gate_up); QFFN_ALIGNED4(stats); QFFN_ALIGNED(dh); QFFN_ALIGNED(gate_up);
+  return from_cuda(qffn::launch_swiglu_backward(d_gate_up, stats, dh, gate_up, N, H, stream));
+}
+
+size_t qffn_backward_qmm_workspace_size(int64_t N, int64_t IC, int64_t OC) {
+  if (check_bqmm_shape(N, IC, OC) != QFFN_OK) return 0;
+  size_t off[5];
+  bqmm_offsets(N, IC, OC, off);
+  return off[4] > 0 ? off[4] : 256;
+}
+
+qffn_status qffn_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout,
+                              const uint16_t* dout, const uint8_t* inp_q, const float* inp_scale,
+                              const uint8_t* w, const float* w_scale, int64_t N, int64_t IC,
+                              int64_t OC, int accumulate, void* workspace, size_t workspace_bytes,
+                              qffn_stream_t stream) {
+  QFFN_PTR(dw); QFFN_PTR(stats_dout); QFFN_PTR(dout); QFFN_PTR(inp_q); QFFN_PTR(inp_scale);
+  QFFN_PTR(w); QFFN_PTR(w_scale); QFFN_PTR(workspace);
+  const qffn_status st = check_bqmm_shape(N, IC, OC);
+  if (st != QFFN_OK) return st;
+  QFFN_REQUIRE(workspace_bytes >= qffn_backward_qmm_workspace_size(N, IC, OC), QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(aligned256(workspace), QFFN_ERR_MISALIGNED);
+  QFFN_ALIGNED(dinp); QFFN_ALIGNED(dw); QFFN_ALIGNED4(stats_dout); QFFN_ALIGNED(dout);
+  QFFN_ALIGNED(inp_q); QFFN_ALIGNED4(inp_scale); QFFN_ALIGNED(w); QFFN_ALIGNED4(w_scale);
+  return from_cuda(run_backward_qmm(dinp, dw, stats_dout, dout, inp_q, inp_scale, w, w_scale, N, IC,
+                                    OC, accumulate != 0, static_cast<uint8_t*>(workspace), stream));
+}
+
+size_t qffn_ffn_backward_workspace_size(int64_t N, int64_t C, int64_t H) {
+  if (check_bqmm_shape(N, H, C) != QFFN_OK || check_bqmm_shape(N, C, 2 * H) != QFFN_OK) return 0;
+  if (H % 128 != 0) return 0;
+  size_t off[5];
+  ffn_bwd_offsets(N, C, H, off);
+  return off[4];
+}
+
+qffn_status qffn_ffn_backward_workspace_offsets(int64_t N, int64_t C, int64_t H,
+                                                size_t offsets[3]) {
+  QFFN_PTR(offsets);
+  if (qffn_ffn_backward_workspace_size(N, C, H) == 0) return QFFN_ERR_UNSUPPORTED_SHAPE;
+  size_t off[5];
+  ffn_bwd_offsets(N, C, H, off);
+  for (int i = 0; i < 3; ++i) offsets[i] = off[i];
+  return QFFN_OK;
+}
+
+qffn_status qffn_ffn_backward(uint16_t* d_ln2, uint16_t* dw1, uint16_t* dw2, float* stats_dout,
+                              float* stats_dgu, const uint16_t* dout, const uint8_t* yq,
+                              const float* y_scale, const uint8_t* hq, const float* h_scale,
+                              const uint8_t* w1, const float* w1_scale, const uint8_t* w2,
+                              const float* w2_scale, int64_t N, int64_t C, int64_t H, int accumulate,
+                              void* workspace, size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_PTR(d_ln2); QFFN_PTR(dw1); QFFN_PTR(dw2); QFFN_PTR(stats_dout); QFFN_PTR(stats_dgu);
+  QFFN_PTR(dout); QFFN_PTR(yq); QFFN_PTR(y_scale); QFFN_PTR(hq); QFFN_PTR(h_scale);
+  QFFN_PTR(w1); QFFN_PTR(w1_scale); QFFN_PTR(w2); QFFN_PTR(w2_scale); QFFN_PTR(workspace);
+  QFFN_REQUIRE(N >= 0 && C >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
+  const size_t need = qffn_ffn_backward_workspace_size(N, C, H);
+  QFFN_REQUIRE(need > 0, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(workspace_bytes >= need, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(aligned256(workspace), QFFN_ERR_MISALIGNED);
+  QFFN_ALIGNED(d_ln2); QFFN_ALIGNED(dw1); QFFN_ALIGNED(dw2); QFFN_ALIGNED4(stats_dout);
+  QFFN_ALIGNED4(stats_dgu); QFFN_ALIGNED(dout); QFFN_ALIGNED(yq); QFFN_ALIGNED4(y_scale);
+  QFFN_ALIGNED(hq); QFFN_ALIGNED4(h_scale); QFFN_ALIGNED(w1); QFFN_ALIGNED4(w1_scale);
+  QFFN_ALIGNED(w2); QFFN_ALIGNED4(w2_scale);
+  size_t off[5];
+  ffn_bwd_offsets(N, C, H, off);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* dh = reinterpret_cast<uint16_t*>(ws + off[0]);
+  uint16_t* gu = reinterpret_cast<uint16_t*>(ws + off[1]);
+  uint16_t* dgu = reinterpret_cast<uint16_t*>(ws + off[2]);
+  uint8_t* bq = ws + off[3];
+  const bool acc = accumulate != 0;
+  // down projection: dh = d(SwiGLU output), dW2
+  QFFN_CUDA(run_backward_qmm(dh, dw2, stats_dout, dout, hq, h_scale, w2, w2_scale, N, H, C, acc, bq,
+                             stream));
+  // recompute the up projection's output (forward_qmm of _recompute_block)
+  QFFN_CUDA(qffn::launch_gemm_bf16(gu, yq, y_scale, w1, w1_scale, N, 2 * H, C, stream));
+  // swiglu_backward with the abs-max of d(gate|up)
+  QFFN_CUDA(qffn::launch_swiglu_backward(dgu, stats_dgu, dh, gu, N, H, stream));
+  // up projection: d_ln2, dW1
+  return from_cuda(run_backward_qmm(d_ln2, dw1, stats_dgu, dgu, yq, y_scale, w1, w1_scale, N, C,
+                                    2 * H, acc, bq, stream));
 }
 
 qffn_status qffn_gemv_dual(uint16_t* g, uint16_t* u, const uint16_t* x, const uint8_t* w_gate,

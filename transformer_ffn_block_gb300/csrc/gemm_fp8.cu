@@ -1,6 +1,6 @@
 // Scaled FP8 (E4M3) GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
 //
-//   gemm_bf16   : out[M,N]  = bf16(sA*sW * A[M,K] . W[N,K]^T (+ bias[N]))
+//   gemm_bf16   : out[M,N]  = bf16(sA*sW * A[M,K] . W[N,K]^T (+ bias[N]) (+ out[M,N]))
 //   gemm_swiglu : h[M,H]    = bf16(silu(g)*u), g / u the bf16-rounded gate and
 //                 up products of W1 = [2H, K] (gate rows [0,H), up rows
 //                 [H,2H)); the tensor abs-max of h is recorded on the way.
@@ -86,6 +86,7 @@ struct GemmArgs {
   const float* w_scale;
   float* amax;   // SwiGLU: stats_h {abs_max, scale}
   const uint16_t* bias;   // bf16 output: optional bf16 bias per output column
+  int accumulate;         // bf16 output: add the previous contents of out (weight gradients)
   int M, N, K;   // N: output columns (SwiGLU: H)
   int H;         // SwiGLU: first up row of W1
   int tiles_m, tiles_n, num_tiles, num_kb;
@@ -390,18 +391,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int col = nb * BN + c0;
           if (row_ok && col < args.N) {
             uint32_t p[16];
-            if (args.bias != nullptr) {
-              // bias added to the scaled accumulator before the one rounding
-              uint32_t bw[16];
+            if (args.bias != nullptr || args.accumulate) {
+              // bias and / or the previous output added to the scaled
+              // accumulator before the one rounding
+              uint32_t bw[16], ow[16];
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const uint4 b4 = ld16_ro(args.bias + col + 8 * j);
+                const uint4 b4 = args.bias != nullptr ? ld16_ro(args.bias + col + 8 * j) : make_uint4(0, 0, 0, 0);
+                const uint4 o4 = args.accumulate ? ld16_once(orow + col + 8 * j) : make_uint4(0, 0, 0, 0);
                 bw[4 * j] = b4.x; bw[4 * j + 1] = b4.y; bw[4 * j + 2] = b4.z; bw[4 * j + 3] = b4.w;
+                ow[4 * j] = o4.x; ow[4 * j + 1] = o4.y; ow[4 * j + 2] = o4.z; ow[4 * j + 3] = o4.w;
               }
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                p[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * scale + bf16_lo(bw[j]),
-                                   __uint_as_float(v[2 * j + 1]) * scale + bf16_hi(bw[j]));
+                p[j] = pack_bf16x2(
+                    (__uint_as_float(v[2 * j]) * scale + bf16_lo(bw[j])) + bf16_lo(ow[j]),
+                    (__uint_as_float(v[2 * j + 1]) * scale + bf16_hi(bw[j])) + bf16_hi(ow[j]));
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
@@ -564,7 +569,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
 
 cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
                              const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
-                             int64_t K, cudaStream_t s, const uint16_t* bias) {
+                             int64_t K, cudaStream_t s, const uint16_t* bias, bool accumulate) {
   if (M == 0) return cudaSuccess;
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, M, K) || !make_map(&mb, W, N, K)) return cudaErrorInvalidValue;
@@ -574,6 +579,7 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.w_scale = w_scale;
   a.amax = nullptr;
   a.bias = bias;
+  a.accumulate = accumulate ? 1 : 0;
   a.M = int(M);
   a.N = int(N);
   a.K = int(K);

@@ -30,11 +30,13 @@ cudaError_t launch_swiglu_requant(uint8_t* hq, float* stats, const uint16_t* gat
 cudaError_t launch_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, bool pdl, cudaStream_t s);
 
 // ---- tcgen05 FP8 GEMMs (gemm_fp8.cu)
-// out[M,N] = bf16(a_scale*w_scale * A[M,K] . W[N,K]^T + bias[N]); bias (bf16,
-// optional) is added to the scaled fp32 accumulator before the rounding.
+// out[M,N] = bf16(a_scale*w_scale * A[M,K] . W[N,K]^T + bias[N] (+ out[M,N])):
+// bias (bf16, optional) and, with `accumulate`, the previous contents of out
+// are added to the scaled fp32 accumulator before the rounding.
 cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
                              const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
-                             int64_t K, cudaStream_t s, const uint16_t* bias = nullptr);
+                             int64_t K, cudaStream_t s, const uint16_t* bias = nullptr,
+                             bool accumulate = false);
 // h[M,H] = bf16(silu(g)*u) with g, u the bf16-rounded gate / up products of
 // W1 = [2H, K]; records max|h| into stats_h[0] (zeroed first).
 cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, const float* a_scale,
@@ -47,6 +49,15 @@ cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t*
                                      int64_t M, int64_t H, int64_t K, cudaStream_t s);
 // Reads and clears the GEMM kernels' device status word of the current device.
 cudaError_t gemm_take_status(unsigned int* status);
+
+// ---- FP8 backward (backward.cu)
+// out[Cc, R] = in[R, Cc]^T for E4M3 codes; R and Cc multiples of 16.
+cudaError_t launch_transpose_u8(uint8_t* out, const uint8_t* in, int64_t R, int64_t Cc,
+                                cudaStream_t s);
+// dgu[N, 2H] = (dh * u * silu'(g) | dh * silu(g)) from gu = [N, 2H] (gate
+// first) and dh [N, H]; records max|dgu| into stats[0] (zeroed first).
+cudaError_t launch_swiglu_backward(uint16_t* dgu, float* stats, const uint16_t* dh,
+                                   const uint16_t* gu, int64_t N, int64_t H, cudaStream_t s);
 
 // ---- decode GEMVs (decode.cu)
 // out0[r] = bf16(s0[r] * W0[r,:] . x); with W1 != NULL also out1 from W1, s1.
