@@ -445,6 +445,78 @@ def bench_attention_projections(q, torch, device, steps, warmup):
     }
 
 
+def bench_backward(q, torch, device, steps, warmup, peaks):
+    """The FP8 FFN backward (qffn_ffn_backward) at the Llama-3-8B shape, fed the
+    forward's quantised activations and a synthetic N(0, 1e-3) output gradient.
+    FLOPs: dgrad and wgrad of both projections (12 N C H) plus the recomputed
+    up projection (4 N C H)."""
+    from ffn_inputs import random_bf16
+    cfg = PREFILL_CFG
+    N, C, H = cfg.N, cfg.C, cfg.H
+    d = prefill_setup(q, torch, device)
+    stream = torch.cuda.Stream(device)
+    forward(q, d, stream)
+    torch.cuda.synchronize()
+    dout = to_dev(random_bf16((N, C), seed=401, std=1e-3), torch, device)
+    st = torch.zeros(4, dtype=torch.float32, device=device)
+    q.qffn_absmax(st[0:2], dout, N * C, stream=stream)
+    d_ln2 = torch.empty(N, C, dtype=torch.int16, device=device)
+    dw1 = torch.empty(2 * H, C, dtype=torch.int16, device=device)
+    dw2 = torch.empty(C, H, dtype=torch.int16, device=device)
+    ws = torch.empty(q.qffn_ffn_backward_workspace_size(N, C, H), dtype=torch.uint8, device=device)
+    off = q.qffn_ffn_backward_workspace_offsets(N, C, H)
+    sy, sh = d["stats"][1:2], d["stats"][3:4]
+
+    def step():
+        q.qffn_ffn_backward(d_ln2, dw1, dw2, st[0:2], st[2:4], dout, d["yq"], sy, d["hq"], sh,
+                            d["w1"], d["w1_scale"], d["w2"], d["w2_scale"], N, C, H, False, ws,
+                            stream=stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    # staged: the four building blocks of the chain with events between them
+    dh = ws[off[0]:].view(torch.int16)
+    gu = ws[off[1]:].view(torch.int16)
+    dgu = ws[off[2]:].view(torch.int16)
+    bq = torch.empty(max(q.qffn_backward_qmm_workspace_size(N, H, C),
+                         q.qffn_backward_qmm_workspace_size(N, C, 2 * H)), dtype=torch.uint8, device=device)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev[0].record(stream)
+    q.qffn_backward_qmm(dh, dw2, st[0:2], dout, d["hq"], sh, d["w2"], d["w2_scale"], N, H, C, False, bq,
+                        stream=stream)
+    ev[1].record(stream)
+    q.qffn_fp8_gemm_scaled(gu, d["yq"], sy, d["w1"], d["w1_scale"], N, 2 * H, C, stream=stream)
+    ev[2].record(stream)
+    q.qffn_swiglu_backward(dgu, st[2:4], dh, gu, N, H, stream=stream)
+    ev[3].record(stream)
+    q.qffn_backward_qmm(d_ln2, dw1, st[2:4], dgu, d["yq"], sy, d["w1"], d["w1_scale"], N, C, 2 * H, False,
+                        bq, stream=stream)
+    ev[4].record(stream)
+    torch.cuda.synchronize()
+    q.qffn_check_status(stream)
+    stage = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+    flop = 16.0 * N * C * H
+    return {
+        "workload": "llama3-8b FFN backward: N=16384, C=4096, H=14336 (down and up backward_qmm, "
+                    "recomputed up projection, swiglu_backward)",
+        "ms_per_step": ms, "tflops": flop / (ms * 1e-3) / 1e12,
+        "tflops_without_recompute": 12.0 * N * C * H / (ms * 1e-3) / 1e12,
+        "launches_per_step": 15,
+        "stages_ms": {"backward_qmm_down": stage[0], "recompute_gate_up": stage[1],
+                      "swiglu_backward": stage[2], "backward_qmm_up": stage[3]},
+        "swiglu_backward_gbs": (2 * N * H * 2 + 2 * N * 2 * H * 2) / (stage[2] * 1e-3) / 1e9,
+    }
+
+
 def bench_decode(q, torch, device, iters, dist, peaks):
     cfg = DECODE_CFG
     C, H = cfg.C, cfg.H
@@ -690,6 +762,7 @@ def main():
     pre = bench_prefill(q, torch, device, args.steps, args.warmup, dist, peaks)
     dec = bench_decode(q, torch, device, args.decode_iters, dist, peaks)
     att = bench_attention_projections(q, torch, device, args.steps, args.warmup)
+    bwd = bench_backward(q, torch, device, max(3, args.steps // 4), args.warmup, peaks)
     cfg = PREFILL_CFG
     value = job_throughput(cfg.gemm_flop, world, pre["ms_per_step"])
     e2e_value = job_throughput(cfg.gemm_flop, world, pre["e2e_ms"])
@@ -711,6 +784,7 @@ def main():
         "down_gemm_tflops": pre["down_gemm_tflops"],
         "recompute": pre["recompute"],
         "attention_projections": att,
+        "backward": bwd,
         "decode": dec,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
