@@ -510,7 +510,7 @@ def bench_backward(q, torch, device, steps, warmup, peaks):
                     "recomputed up projection, swiglu_backward)",
         "ms_per_step": ms, "tflops": flop / (ms * 1e-3) / 1e12,
         "tflops_without_recompute": 12.0 * N * C * H / (ms * 1e-3) / 1e12,
-        "launches_per_step": 15,
+        "launches_per_step": 8,
         "stages_ms": {"backward_qmm_down": stage[0], "recompute_gate_up": stage[1],
                       "swiglu_backward": stage[2], "backward_qmm_up": stage[3]},
         "swiglu_backward_gbs": (2 * N * H * 2 + 2 * N * 2 * H * 2) / (stage[2] * 1e-3) / 1e9,

@@ -228,8 +228,9 @@ qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd
  * Gradients are bf16; their FP8 copies are E4M3 quantised with a recorded
  * abs-max, exactly as activations are (qffn_quantize). */
 
-/* E4M3 transpose: out[cols, rows] = in[rows, cols]^T (backward_qmm's
- * transpose of the weight and of the quantised operands).  rows and cols are
+/* E4M3 transpose: out[cols, rows] = in[rows, cols]^T, the transpose the
+ * page's backward_qmm applies to the weight and to the quantised operands
+ * (qffn_backward_qmm itself reads them MN-major instead).  rows and cols are
  * multiples of 16; rows < 64 * 65535. */
 qffn_status qffn_transpose_e4m3(uint8_t* out, const uint8_t* in, int64_t rows, int64_t cols,
                                 qffn_stream_t stream);
@@ -253,10 +254,11 @@ qffn_status qffn_swiglu_backward(uint16_t* d_gate_up, float* stats, const uint16
  *   dw[OC, IC]  = bf16(stats_dout[1] * inp_scale * sum_n dq[n, oc] * inp_q[n, ic]
  *                      (+ dw[OC, IC] when accumulate != 0))
  * stats_dout[0] is the recorded abs-max of dout (an input).  dinp may be NULL
- * (weight gradient only).  As on the page, the weight and both operands of
- * the weight gradient are transposed into the workspace so that each matmul
- * is K-contiguous.  workspace: >= qffn_backward_qmm_workspace_size() bytes,
- * 256-byte aligned.  N % 16 == 0, IC % 32 == 0, OC % 32 == 0 (all >= 32
+ * (weight gradient only).  The page transposes the weight and both operands
+ * of the weight gradient so that each matmul is K-contiguous; here the tensor
+ * cores read W, dq and inp_q MN-major where they lie, and the workspace holds
+ * only dq.  workspace: >= qffn_backward_qmm_workspace_size() bytes, 256-byte
+ * aligned; dq [N, OC] is at offset 0 after the call.  N % 16 == 0, IC % 32 == 0, OC % 32 == 0 (all >= 32
  * except N >= 0), IC, OC <= 2^20. */
 size_t qffn_backward_qmm_workspace_size(int64_t N, int64_t IC, int64_t OC);
 qffn_status qffn_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout,

@@ -44,27 +44,24 @@ void forward_offsets(int64_t N, int64_t C, int64_t H, size_t off[5]) {
   off[4] = round_up(off[3] + size_t(N) * size_t(H), 256);
 }
 
-// backward_qmm workspace: dout_q [N,OC] | dout_q^T [OC,N] | inp_q^T [IC,N] | W^T [IC,OC],
-// E4M3, each 256-byte aligned
-void bqmm_offsets(int64_t N, int64_t IC, int64_t OC, size_t off[5]) {
+// backward_qmm workspace: dout_q [N,OC] E4M3
+void bqmm_offsets(int64_t N, int64_t IC, int64_t OC, size_t off[2]) {
+  (void)IC;
   off[0] = 0;
-  off[1] = round_up(off[0] + size_t(N) * size_t(OC), 256);
-  off[2] = round_up(off[1] + size_t(OC) * size_t(N), 256);
-  off[3] = round_up(off[2] + size_t(IC) * size_t(N), 256);
-  off[4] = round_up(off[3] + size_t(IC) * size_t(OC), 256);
+  off[1] = round_up(size_t(N) * size_t(OC), 256);
 }
 
 // FFN backward workspace: dh [N,H] bf16 | gu [N,2H] bf16 | d_gu [N,2H] bf16 |
 // the larger of the two backward_qmm workspaces
 void ffn_bwd_offsets(int64_t N, int64_t C, int64_t H, size_t off[5]) {
-  size_t down[5], up[5];
+  size_t down[2], up[2];
   bqmm_offsets(N, H, C, down);
   bqmm_offsets(N, C, 2 * H, up);
   off[0] = 0;
   off[1] = round_up(size_t(N) * size_t(H) * 2, 256);
   off[2] = round_up(off[1] + size_t(N) * size_t(2 * H) * 2, 256);
   off[3] = round_up(off[2] + size_t(N) * size_t(2 * H) * 2, 256);
-  off[4] = off[3] + (down[4] > up[4] ? down[4] : up[4]);
+  off[4] = off[3] + (down[1] > up[1] ? down[1] : up[1]);
 }
 
 qffn_status check_bqmm_shape(int64_t N, int64_t IC, int64_t OC) {
@@ -75,33 +72,28 @@ qffn_status check_bqmm_shape(int64_t N, int64_t IC, int64_t OC) {
   return QFFN_OK;
 }
 
-// The FP8 branch of backward_qmm on pointers already checked; ws holds bqmm_offsets.
+// The FP8 branch of backward_qmm on pointers already checked; ws holds dout_q.
+// The page transposes W, dout_q and inp_q so that both matmuls are
+// K-contiguous; here the tensor cores read them MN-major where they lie.
 cudaError_t run_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout, const uint16_t* dout,
                              const uint8_t* inp_q, const float* inp_scale, const uint8_t* w,
                              const float* w_scale, int64_t N, int64_t IC, int64_t OC,
                              bool accumulate, uint8_t* ws, cudaStream_t s) {
-  size_t off[5];
-  bqmm_offsets(N, IC, OC, off);
-  uint8_t* dq = ws + off[0];
-  uint8_t* dqt = ws + off[1];
-  uint8_t* inpt = ws + off[2];
-  uint8_t* wt = ws + off[3];
+  uint8_t* dq = ws;
   cudaError_t e;
   // quantize_with_abs_max(dout.Quant, scale, dout.Value, dout.Quant.abs_max())
   if ((e = qffn::launch_quantize(dq, stats_dout, dout, N * OC, s)) != cudaSuccess) return e;
   if (dinp != nullptr) {
-    // dinp[N,IC] = dout_q[N,OC] . (W^T)[IC,OC]^T, scales W.scale * dout.scale
-    if ((e = qffn::launch_transpose_u8(wt, w, OC, IC, s)) != cudaSuccess) return e;
-    if ((e = qffn::launch_gemm_bf16(dinp, dq, stats_dout + 1, wt, w_scale, N, IC, OC, s)) != cudaSuccess)
+    // dinp[N,IC] = dout_q[N,OC] . W[OC,IC], scales W.scale * dout.scale (W read MN-major)
+    if ((e = qffn::launch_gemm_bf16(dinp, dq, stats_dout + 1, w, w_scale, N, IC, OC, s, nullptr,
+                                    false, false, true)) != cudaSuccess)
       return e;
   }
   // no tokens: the weight gradient is a sum over nothing (0, or unchanged when accumulating)
   if (N == 0) return accumulate ? cudaSuccess : cudaMemsetAsync(dw, 0, size_t(OC) * size_t(IC) * 2, s);
-  // dW[OC,IC] (+)= (dout_q^T)[OC,N] . (inp_q^T)[IC,N]^T, scales inp.scale * dout.scale
-  if ((e = qffn::launch_transpose_u8(dqt, dq, N, OC, s)) != cudaSuccess) return e;
-  if ((e = qffn::launch_transpose_u8(inpt, inp_q, N, IC, s)) != cudaSuccess) return e;
-  return qffn::launch_gemm_bf16(dw, dqt, stats_dout + 1, inpt, inp_scale, OC, IC, N, s, nullptr,
-                                accumulate);
+  // dW[OC,IC] (+)= dout_q[N,OC]^T . inp_q[N,IC], scales inp.scale * dout.scale (both MN-major)
+  return qffn::launch_gemm_bf16(dw, dq, stats_dout + 1, inp_q, inp_scale, OC, IC, N, s, nullptr,
+                                accumulate, true, true);
 }
 
 // decode workspace: g [H] bf16 | u [H] bf16, each 256-byte aligned
@@ -384,9 +376,9 @@ qffn_status qffn_swiglu_backward(uint16_t* d_gate_up, float* stats, const uint16
 
 size_t qffn_backward_qmm_workspace_size(int64_t N, int64_t IC, int64_t OC) {
   if (check_bqmm_shape(N, IC, OC) != QFFN_OK) return 0;
-  size_t off[5];
+  size_t off[2];
   bqmm_offsets(N, IC, OC, off);
-  return off[4] > 0 ? off[4] : 256;
+  return off[1] > 0 ? off[1] : 256;
 }
 
 qffn_status qffn_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout,

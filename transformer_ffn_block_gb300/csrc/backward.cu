@@ -1,10 +1,12 @@
 // HBM-bound kernels of the FP8 FFN backward (llmq "llama_model.cpp",
 // _backward_block and the FP8 branch of backward_qmm):
 //
-//   transpose_u8_kernel      E4M3 matrix transpose.  backward_qmm transposes the
-//                            weight for the input gradient and both quantised
-//                            operands of the weight gradient, so every matmul
-//                            stays a K-contiguous ("TN") product.
+//   transpose_u8_kernel      E4M3 matrix transpose: the page's backward_qmm
+//                            transposes the weight for the input gradient and
+//                            both quantised operands of the weight gradient so
+//                            that every matmul is K-contiguous.  The library's
+//                            backward reads those operands MN-major in the
+//                            GEMM instead; the transpose stays available.
 //   swiglu_backward_kernel   gradient of h = silu(g) * u w.r.t. the fused
 //                            gate|up output, with its tensor abs-max.
 #include "common.cuh"

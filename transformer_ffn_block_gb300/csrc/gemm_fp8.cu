@@ -31,6 +31,13 @@
 //               scaling, bf16 rounding, SwiGLU, abs-max, 16-byte stores; the
 //               accumulator is handed back to the leader's MMA thread by a
 //               remote mbarrier arrive.
+// Operands are K-major (K contiguous, "TN") by default.  The bf16 form also
+// reads A and / or W MN-major (the M or N index contiguous, i.e. the
+// transposed matrix as it lies in memory): the TMA box is then 128 bytes of
+// M (N) by 128 rows of K, which in the 128-byte swizzle is the canonical
+// MN-major layout with one swizzle atom along M (N) per CTA, and the MMA
+// reads it with the operand's major-ness bit set.  The FP8 backward uses it
+// for W^T in the input gradient and for both operands of the weight gradient.
 // Two 256-column accumulators in TMEM let the epilogue of tile i overlap the
 // MMAs of tile i+1.  In the SwiGLU form CTA 0 stages 128 gate rows and CTA 1
 // the matching 128 up rows, so the accumulator holds gate in columns
@@ -72,6 +79,14 @@ constexpr unsigned long long kDrainLimitNs = 200000000ull;
 // A and B E4M3 (bits 7-9, 10-12 = 0), both K-major (bits 15, 16 = 0),
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28 (M = 256 over the CTA pair).
 constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t((2 * BM) >> 4) << 24);
+// Bits 15 / 16: A / B read MN-major.
+constexpr uint32_t idesc_for(bool a_mn, bool b_mn) {
+  return kIdesc | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
+}
+// Byte step of one UMMA_K slice inside a stage: along the 128-byte row for a
+// K-major operand, UMMA_K rows of 128 bytes for an MN-major one.
+constexpr uint32_t kStepK = UMMA_K;
+constexpr uint32_t kStepMN = UMMA_K * 128;
 
 __device__ unsigned int g_status;
 
@@ -185,11 +200,12 @@ QFFN_DEVI uint64_t sdesc_sw128(uint32_t saddr) {
 }
 
 // D(tmem, both CTAs) (+)= A(smem, both CTAs) . B(smem, both CTAs)^T
-QFFN_DEVI void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+QFFN_DEVI void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                            uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 // Arrive once on the barrier at offset `bar` of every CTA in `mask` when all
@@ -232,7 +248,7 @@ QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
   nb = r / gsize;
 }
 
-template <int EPI>
+template <int EPI, bool A_MN = false, bool B_MN = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs args) {
@@ -309,8 +325,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
           if (rank == 0) mbar_expect_tx(full_bar(s), 2 * STAGE_BYTES);
           const uint32_t fb = map_to_rank(full_bar(s), 0);
-          tma_load_2d_pair(smem_u32(sA + s * A_BYTES), &tmA, fb, kb * BK, rowA);
-          tma_load_2d_pair(smem_u32(sB + s * B_BYTES), &tmB, fb, kb * BK, rowB);
+          // K-major: x = K offset, y = row; MN-major: x = M (N) offset, y = K row
+          if (A_MN) tma_load_2d_pair(smem_u32(sA + s * A_BYTES), &tmA, fb, rowA, kb * BK);
+          else tma_load_2d_pair(smem_u32(sA + s * A_BYTES), &tmA, fb, kb * BK, rowA);
+          if (B_MN) tma_load_2d_pair(smem_u32(sB + s * B_BYTES), &tmB, fb, rowB, kb * BK);
+          else tma_load_2d_pair(smem_u32(sB + s * B_BYTES), &tmB, fb, kb * BK, rowB);
           issued |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
         }
@@ -343,7 +362,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b0 = smem_u32(sB + s * B_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk)
-            mma_f8_pair(d_tmem, sdesc_sw128(a0 + kk * UMMA_K), sdesc_sw128(b0 + kk * UMMA_K),
+            mma_f8_pair(d_tmem, sdesc_sw128(a0 + kk * (A_MN ? kStepMN : kStepK)),
+                        sdesc_sw128(b0 + kk * (B_MN ? kStepMN : kStepK)), idesc_for(A_MN, B_MN),
                         uint32_t(kb | kk));
           mma_commit_mc(empty_bar(s), kBothCtas);
         }
@@ -511,7 +531,7 @@ bool make_map(CUtensorMap* map, const uint8_t* ptr, int64_t rows, int64_t k) {
 
 // Number of 2-CTA clusters of this kernel that fit on the device at once
 // (cached per device and form).
-template <int EPI>
+template <int EPI, bool A_MN = false, bool B_MN = false>
 cudaError_t max_pairs(int* pairs) {
   static int cached[64] = {0};
   int dev = 0;
@@ -521,7 +541,7 @@ cudaError_t max_pairs(int* pairs) {
     *pairs = cached[dev];
     return cudaSuccess;
   }
-  e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -536,7 +556,7 @@ cudaError_t max_pairs(int* pairs) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI, A_MN, B_MN>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
   if (dev >= 0 && dev < 64) cached[dev] = n;
@@ -544,10 +564,10 @@ cudaError_t max_pairs(int* pairs) {
   return cudaSuccess;
 }
 
-template <int EPI>
+template <int EPI, bool A_MN = false, bool B_MN = false>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s) {
   int pairs = 0;
-  cudaError_t e = max_pairs<EPI>(&pairs);
+  cudaError_t e = max_pairs<EPI, A_MN, B_MN>(&pairs);
   if (e != cudaSuccess) return e;
   if (a.num_tiles < pairs) pairs = a.num_tiles;
   cudaLaunchConfig_t cfg = {};
@@ -562,17 +582,21 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI>, ma, mb, a);
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, A_MN, B_MN>, ma, mb, a);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
                              const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
-                             int64_t K, cudaStream_t s, const uint16_t* bias, bool accumulate) {
+                             int64_t K, cudaStream_t s, const uint16_t* bias, bool accumulate,
+                             bool a_mn, bool w_mn) {
   if (M == 0) return cudaSuccess;
   CUtensorMap ma, mb;
-  if (!make_map(&ma, A, M, K) || !make_map(&mb, W, N, K)) return cudaErrorInvalidValue;
+  // an MN-major operand lies in memory as [K rows, M (N) contiguous]
+  const bool ok = (a_mn ? make_map(&ma, A, K, M) : make_map(&ma, A, M, K)) &&
+                  (w_mn ? make_map(&mb, W, K, N) : make_map(&mb, W, N, K));
+  if (!ok) return cudaErrorInvalidValue;
   GemmArgs a{};
   a.out = out;
   a.a_scale = a_scale;
@@ -588,6 +612,9 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.tiles_n = int((N + BN - 1) / BN);
   a.num_tiles = a.tiles_m * a.tiles_n;
   a.num_kb = int((K + BK - 1) / BK);
+  if (a_mn && w_mn) return launch<EPI_BF16, true, true>(ma, mb, a, s);
+  if (a_mn) return launch<EPI_BF16, true, false>(ma, mb, a, s);
+  if (w_mn) return launch<EPI_BF16, false, true>(ma, mb, a, s);
   return launch<EPI_BF16>(ma, mb, a, s);
 }
 

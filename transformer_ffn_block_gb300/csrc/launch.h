@@ -32,11 +32,13 @@ cudaError_t launch_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, bool pdl,
 // ---- tcgen05 FP8 GEMMs (gemm_fp8.cu)
 // out[M,N] = bf16(a_scale*w_scale * A[M,K] . W[N,K]^T + bias[N] (+ out[M,N])):
 // bias (bf16, optional) and, with `accumulate`, the previous contents of out
-// are added to the scaled fp32 accumulator before the rounding.
+// are added to the scaled fp32 accumulator before the rounding.  With a_mn
+// (w_mn) the operand is given MN-major, i.e. A as [K, M] (W as [K, N]) with
+// the M (N) index contiguous; M (N) must then be a multiple of 16.
 cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
                              const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
                              int64_t K, cudaStream_t s, const uint16_t* bias = nullptr,
-                             bool accumulate = false);
+                             bool accumulate = false, bool a_mn = false, bool w_mn = false);
 // h[M,H] = bf16(silu(g)*u) with g, u the bf16-rounded gate / up products of
 // W1 = [2H, K]; records max|h| into stats_h[0] (zeroed first).
 cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, const float* a_scale,
