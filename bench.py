@@ -483,37 +483,35 @@ def bench_backward(q, torch, device, steps, warmup, peaks):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    # staged: the four building blocks of the chain with events between them
+    # staged: the three building blocks of the chain with events between them
     dh = ws[off[0]:].view(torch.int16)
-    gu = ws[off[1]:].view(torch.int16)
-    dgu = ws[off[2]:].view(torch.int16)
+    dgu = ws[off[1]:].view(torch.int16)
     bq = torch.empty(max(q.qffn_backward_qmm_workspace_size(N, H, C),
                          q.qffn_backward_qmm_workspace_size(N, C, 2 * H)), dtype=torch.uint8, device=device)
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     ev[0].record(stream)
     q.qffn_backward_qmm(dh, dw2, st[0:2], dout, d["hq"], sh, d["w2"], d["w2_scale"], N, H, C, False, bq,
                         stream=stream)
     ev[1].record(stream)
-    q.qffn_fp8_gemm_scaled(gu, d["yq"], sy, d["w1"], d["w1_scale"], N, 2 * H, C, stream=stream)
+    q.qffn_gate_up_swiglu_backward(dgu, st[2:4], dh, d["yq"], sy, d["w1"], d["w1_scale"], N, C, H,
+                                   stream=stream)
     ev[2].record(stream)
-    q.qffn_swiglu_backward(dgu, st[2:4], dh, gu, N, H, stream=stream)
-    ev[3].record(stream)
     q.qffn_backward_qmm(d_ln2, dw1, st[2:4], dgu, d["yq"], sy, d["w1"], d["w1_scale"], N, C, 2 * H, False,
                         bq, stream=stream)
-    ev[4].record(stream)
+    ev[3].record(stream)
     torch.cuda.synchronize()
     q.qffn_check_status(stream)
-    stage = [ev[i].elapsed_time(ev[i + 1]) for i in range(4)]
+    stage = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
     flop = 16.0 * N * C * H
     return {
         "workload": "llama3-8b FFN backward: N=16384, C=4096, H=14336 (down and up backward_qmm, "
-                    "recomputed up projection, swiglu_backward)",
+                    "recomputed up projection fused with swiglu_backward)",
         "ms_per_step": ms, "tflops": flop / (ms * 1e-3) / 1e12,
         "tflops_without_recompute": 12.0 * N * C * H / (ms * 1e-3) / 1e12,
-        "launches_per_step": 8,
-        "stages_ms": {"backward_qmm_down": stage[0], "recompute_gate_up": stage[1],
-                      "swiglu_backward": stage[2], "backward_qmm_up": stage[3]},
-        "swiglu_backward_gbs": (2 * N * H * 2 + 2 * N * 2 * H * 2) / (stage[2] * 1e-3) / 1e9,
+        "launches_per_step": 7,
+        "stages_ms": {"backward_qmm_down": stage[0], "gate_up_swiglu_backward": stage[1],
+                      "backward_qmm_up": stage[2]},
+        "gate_up_swiglu_backward_tflops": 2.0 * N * C * 2 * H / (stage[1] * 1e-3) / 1e12,
     }
 
 

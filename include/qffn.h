@@ -267,24 +267,36 @@ qffn_status qffn_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout,
                               int64_t OC, int accumulate, void* workspace, size_t workspace_bytes,
                               qffn_stream_t stream);
 
+/* Recompute of the up projection fused with swiglu_backward: the gate|up
+ * GEMM of qffn_gate_up_swiglu, whose epilogue rounds g and u to bf16 (the
+ * recomputed mlp_up buffer of _recompute_block), reads dh [N, H] and writes
+ * d_gate_up [N, 2H] and stats[0] = max |d_gate_up| (zeroed first) exactly as
+ * qffn_fp8_gemm_scaled into [N, 2H] followed by qffn_swiglu_backward would.
+ * The [N, 2H] gate|up product is never written.  Shape rules of
+ * qffn_gate_up_swiglu. */
+qffn_status qffn_gate_up_swiglu_backward(uint16_t* d_gate_up, float* stats, const uint16_t* dh,
+                                         const uint8_t* yq, const float* y_scale,
+                                         const uint8_t* w1, const float* w1_scale, int64_t N,
+                                         int64_t C, int64_t H, qffn_stream_t stream);
+
 /* The FFN half of _backward_block after the norm, for the block output
  * gradient dout [N, C] (bf16, stats_dout[0] = its recorded abs-max):
  *   1. backward_qmm of the down projection (inp = hq [N, H] of the forward,
  *      W2 [C, H]) -> dh [N, H], dw2 [C, H];
- *   2. the up projection's output gate_up [N, 2H] recomputed from yq and W1
- *      (forward_qmm of _recompute_block);
- *   3. swiglu_backward -> d_gate_up [N, 2H], stats_dgu[0] = its abs-max;
- *   4. backward_qmm of the up projection (inp = yq [N, C], W1 [2H, C])
+ *   2. the up projection's output recomputed from yq and W1 (forward_qmm of
+ *      _recompute_block) and swiglu_backward on it, fused
+ *      (qffn_gate_up_swiglu_backward) -> d_gate_up [N, 2H], stats_dgu[0];
+ *   3. backward_qmm of the up projection (inp = yq [N, C], W1 [2H, C])
  *      -> d_ln2 [N, C], dw1 [2H, C].
  * stats_dout[1] and stats_dgu[1] receive the two gradient scales.  With
  * accumulate != 0 the weight gradients add to dw1 and dw2.  workspace: >=
  * qffn_ffn_backward_workspace_size() bytes, 256-byte aligned; after the call
- * it holds dh, gate_up and d_gate_up (bf16) at the offsets that
- * qffn_ffn_backward_workspace_offsets() returns.  N % 16 == 0,
- * C % 32 == 0, H % 128 == 0, C, H >= 128. */
+ * it holds dh and d_gate_up (bf16) at the offsets that
+ * qffn_ffn_backward_workspace_offsets() returns.  Seven kernels.
+ * N % 16 == 0, C % 32 == 0, H % 128 == 0, C, H >= 128. */
 size_t qffn_ffn_backward_workspace_size(int64_t N, int64_t C, int64_t H);
 qffn_status qffn_ffn_backward_workspace_offsets(int64_t N, int64_t C, int64_t H,
-                                                size_t offsets[3] /* dh, gate_up, d_gate_up */);
+                                                size_t offsets[2] /* dh, d_gate_up */);
 qffn_status qffn_ffn_backward(uint16_t* d_ln2, uint16_t* dw1, uint16_t* dw2, float* stats_dout,
                               float* stats_dgu, const uint16_t* dout, const uint8_t* yq,
                               const float* y_scale, const uint8_t* hq, const float* h_scale,

@@ -172,7 +172,8 @@ def test_backward_checks(lib):
     assert lib.qffn_ffn_backward_workspace_size(64, 256, 768) > 0
     assert lib.qffn_ffn_backward_workspace_size(64, 256, 200) == 0          # H % 128
     off = lib.qffn_ffn_backward_workspace_offsets(64, 256, 768)
-    assert off[0] == 0 and off[1] >= 64 * 768 * 2 and off[2] >= off[1] + 64 * 1536 * 2
+    assert off[0] == 0 and off[1] >= 64 * 768 * 2
+    assert lib.qffn_ffn_backward_workspace_size(64, 256, 768) >= off[1] + 64 * 1536 * 2
     assert all(o % 256 == 0 for o in off)
     assert _call(lib, "qffn_transpose_e4m3", A, A, 24, 16, None) == 2
     assert _call(lib, "qffn_transpose_e4m3", MIS, A, 16, 16, None) == 3

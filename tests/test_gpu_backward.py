@@ -102,15 +102,42 @@ def _ffn_backward_dev(q, dout, amax, yq, sy, hq, sh, w1q, w1s, w2q, w2s, N, C, H
     q.qffn_check_status()
     sync()
     off = q.qffn_ffn_backward_workspace_offsets(N, C, H)
-    return dict(d_ln2=d_ln2, dw1=dw1, dw2=dw2, st=host(st),
+    # the recomputed gate|up product is not kept by the chain: the unfused GEMM makes it
+    gu = empty_bf16(N, 2 * H)
+    q.qffn_fp8_gemm_scaled(gu, dev(yq), sc[0:1], dev(w1q), sc[2:3], N, 2 * H, C)
+    sync()
+    return dict(d_ln2=d_ln2, dw1=dw1, dw2=dw2, st=host(st), gu=gu,
                 dh=ws[off[0]:off[0] + N * H * 2].view(torch.int16).view(N, H),
-                gu=ws[off[1]:off[1] + N * 2 * H * 2].view(torch.int16).view(N, 2 * H),
-                dgu=ws[off[2]:off[2] + N * 2 * H * 2].view(torch.int16).view(N, 2 * H))
+                dgu=ws[off[1]:off[1] + N * 2 * H * 2].view(torch.int16).view(N, 2 * H))
 
 
 def _ffn_backward_gpu(*a, **k):
     g = _ffn_backward_dev(*a, **k)
     return {key: (v if key == "st" else bf(v)) for key, v in g.items()}
+
+
+@pytest.mark.parametrize("N,C,H", [(64, 256, 768), (1, 128, 128), (200, 384, 256), (513, 2048, 1024)])
+def test_gate_up_swiglu_backward_equals_unfused(q, N, C, H):
+    """The fused recompute + swiglu_backward equals the unfused GEMM into [N, 2H]
+    followed by qffn_swiglu_backward, bit for bit, abs-max included."""
+    yq, sy = oracle.quantize_tensor(random_bf16((N, C), seed=N + C))
+    w1q, w1s = oracle.quantize_tensor(random_bf16((2 * H, C), seed=H + C, std=0.02))
+    dh = random_bf16((N, H), seed=N + H, std=1e-3)
+    sc = torch.tensor([sy, w1s], dtype=torch.float32, device="cuda")
+    yqd, w1d, dhd = dev(yq), dev(w1q), dev(dh)
+    gu = empty_bf16(N, 2 * H)
+    q.qffn_fp8_gemm_scaled(gu, yqd, sc[0:1], w1d, sc[1:2], N, 2 * H, C)
+    d_ref = empty_bf16(N, 2 * H)
+    st_ref = torch.zeros(2, dtype=torch.float32, device="cuda")
+    q.qffn_swiglu_backward(d_ref, st_ref, dhd, gu, N, H)
+    d = empty_bf16(N, 2 * H)
+    st = torch.full((2,), 3.0, dtype=torch.float32, device="cuda")
+    q.qffn_gate_up_swiglu_backward(d, st, dhd, yqd, sc[0:1], w1d, sc[1:2], N, C, H)
+    q.qffn_check_status()
+    sync()
+    np.testing.assert_array_equal(bf(d), bf(d_ref))
+    assert host(st)[0] == host(st_ref)[0] and host(st)[1] == 3.0
+    _check_swiglu_grad(bf(d), oracle.swiglu_backward(dh, bf(gu), H)[0])
 
 
 def _backward_inputs(N, C, H, seed):

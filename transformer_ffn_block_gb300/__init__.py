@@ -24,7 +24,7 @@ __all__ = [
     "qffn_forward_workspace_size", "qffn_forward_workspace_offsets", "qffn_forward",
     "qffn_forward_recompute", "qffn_transpose_e4m3", "qffn_swiglu_backward",
     "qffn_backward_qmm_workspace_size", "qffn_backward_qmm", "qffn_ffn_backward_workspace_size",
-    "qffn_ffn_backward_workspace_offsets", "qffn_ffn_backward",
+    "qffn_ffn_backward_workspace_offsets", "qffn_ffn_backward", "qffn_gate_up_swiglu_backward",
     "qffn_gemv_dual", "qffn_gemv", "qffn_gemv_silu_input", "qffn_silu_mul", "qffn_decode_workspace_size",
     "qffn_decode_forward", "qffn_decode_forward_noalloc",
 ]
@@ -70,6 +70,7 @@ _SIGS = {
     "qffn_backward_qmm_workspace_size": ([_I64, _I64, _I64], _SZ),
     "qffn_backward_qmm": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _S, _P, _SZ, _P], _S),
     "qffn_ffn_backward_workspace_size": ([_I64, _I64, _I64], _SZ),
+    "qffn_gate_up_swiglu_backward": ([_P, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _S),
     "qffn_ffn_backward_workspace_offsets": ([_I64, _I64, _I64, ctypes.POINTER(_SZ)], _S),
     "qffn_ffn_backward": ([_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                            _I64, _I64, _I64, _S, _P, _SZ, _P], _S),
@@ -241,8 +242,15 @@ def qffn_ffn_backward_workspace_size(N, C, H) -> int:
     return int(lib.qffn_ffn_backward_workspace_size(int(N), int(C), int(H)))
 
 
+def qffn_gate_up_swiglu_backward(d_gate_up, stats, dh, yq, y_scale, w1, w1_scale, N, C, H,
+                                 stream=None):
+    _check("qffn_gate_up_swiglu_backward", lib.qffn_gate_up_swiglu_backward(
+        _ptr(d_gate_up), _ptr(stats), _ptr(dh), _ptr(yq), _ptr(y_scale), _ptr(w1), _ptr(w1_scale),
+        int(N), int(C), int(H), _stream(stream)))
+
+
 def qffn_ffn_backward_workspace_offsets(N, C, H) -> list[int]:
-    off = (_SZ * 3)()
+    off = (_SZ * 2)()
     _check("qffn_ffn_backward_workspace_offsets",
            lib.qffn_ffn_backward_workspace_offsets(int(N), int(C), int(H), off))
     return [int(v) for v in off]

@@ -51,17 +51,16 @@ void bqmm_offsets(int64_t N, int64_t IC, int64_t OC, size_t off[2]) {
   off[1] = round_up(size_t(N) * size_t(OC), 256);
 }
 
-// FFN backward workspace: dh [N,H] bf16 | gu [N,2H] bf16 | d_gu [N,2H] bf16 |
-// the larger of the two backward_qmm workspaces
-void ffn_bwd_offsets(int64_t N, int64_t C, int64_t H, size_t off[5]) {
+// FFN backward workspace: dh [N,H] bf16 | d_gu [N,2H] bf16 | the larger of the
+// two backward_qmm workspaces
+void ffn_bwd_offsets(int64_t N, int64_t C, int64_t H, size_t off[4]) {
   size_t down[2], up[2];
   bqmm_offsets(N, H, C, down);
   bqmm_offsets(N, C, 2 * H, up);
   off[0] = 0;
   off[1] = round_up(size_t(N) * size_t(H) * 2, 256);
   off[2] = round_up(off[1] + size_t(N) * size_t(2 * H) * 2, 256);
-  off[3] = round_up(off[2] + size_t(N) * size_t(2 * H) * 2, 256);
-  off[4] = off[3] + (down[1] > up[1] ? down[1] : up[1]);
+  off[3] = off[2] + (down[1] > up[1] ? down[1] : up[1]);
 }
 
 qffn_status check_bqmm_shape(int64_t N, int64_t IC, int64_t OC) {
@@ -401,19 +400,36 @@ qffn_status qffn_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout,
 size_t qffn_ffn_backward_workspace_size(int64_t N, int64_t C, int64_t H) {
   if (check_bqmm_shape(N, H, C) != QFFN_OK || check_bqmm_shape(N, C, 2 * H) != QFFN_OK) return 0;
   if (H % 128 != 0) return 0;
-  size_t off[5];
+  size_t off[4];
   ffn_bwd_offsets(N, C, H, off);
-  return off[4];
+  return off[3];
 }
 
 qffn_status qffn_ffn_backward_workspace_offsets(int64_t N, int64_t C, int64_t H,
-                                                size_t offsets[3]) {
+                                                size_t offsets[2]) {
   QFFN_PTR(offsets);
   if (qffn_ffn_backward_workspace_size(N, C, H) == 0) return QFFN_ERR_UNSUPPORTED_SHAPE;
-  size_t off[5];
+  size_t off[4];
   ffn_bwd_offsets(N, C, H, off);
-  for (int i = 0; i < 3; ++i) offsets[i] = off[i];
+  for (int i = 0; i < 2; ++i) offsets[i] = off[i];
   return QFFN_OK;
+}
+
+qffn_status qffn_gate_up_swiglu_backward(uint16_t* d_gate_up, float* stats, const uint16_t* dh,
+                                         const uint8_t* yq, const float* y_scale,
+                                         const uint8_t* w1, const float* w1_scale, int64_t N,
+                                         int64_t C, int64_t H, qffn_stream_t stream) {
+  QFFN_PTR(d_gate_up); QFFN_PTR(stats); QFFN_PTR(dh); QFFN_PTR(yq); QFFN_PTR(y_scale);
+  QFFN_PTR(w1); QFFN_PTR(w1_scale);
+  QFFN_REQUIRE(N >= 0 && C >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(C % 16 == 0 && C >= 16 && C <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE(H % 128 == 0 && H >= 128 && H <= kMaxDim, QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_REQUIRE((N + 127) / 128 * (H / 128) < (int64_t(1) << 31), QFFN_ERR_UNSUPPORTED_SHAPE);
+  QFFN_ALIGNED(d_gate_up); QFFN_ALIGNED4(stats); QFFN_ALIGNED(dh); QFFN_ALIGNED(yq);
+  QFFN_ALIGNED4(y_scale); QFFN_ALIGNED(w1); QFFN_ALIGNED4(w1_scale);
+  return from_cuda(qffn::launch_gemm_swiglu_bwd(d_gate_up, stats, dh, yq, y_scale, w1, w1_scale, N,
+                                                H, C, stream));
 }
 
 qffn_status qffn_ffn_backward(uint16_t* d_ln2, uint16_t* dw1, uint16_t* dw2, float* stats_dout,
@@ -434,21 +450,20 @@ qffn_status qffn_ffn_backward(uint16_t* d_ln2, uint16_t* dw1, uint16_t* dw2, flo
   QFFN_ALIGNED4(stats_dgu); QFFN_ALIGNED(dout); QFFN_ALIGNED(yq); QFFN_ALIGNED4(y_scale);
   QFFN_ALIGNED(hq); QFFN_ALIGNED4(h_scale); QFFN_ALIGNED(w1); QFFN_ALIGNED4(w1_scale);
   QFFN_ALIGNED(w2); QFFN_ALIGNED4(w2_scale);
-  size_t off[5];
+  size_t off[4];
   ffn_bwd_offsets(N, C, H, off);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint16_t* dh = reinterpret_cast<uint16_t*>(ws + off[0]);
-  uint16_t* gu = reinterpret_cast<uint16_t*>(ws + off[1]);
-  uint16_t* dgu = reinterpret_cast<uint16_t*>(ws + off[2]);
-  uint8_t* bq = ws + off[3];
+  uint16_t* dgu = reinterpret_cast<uint16_t*>(ws + off[1]);
+  uint8_t* bq = ws + off[2];
   const bool acc = accumulate != 0;
   // down projection: dh = d(SwiGLU output), dW2
   QFFN_CUDA(run_backward_qmm(dh, dw2, stats_dout, dout, hq, h_scale, w2, w2_scale, N, H, C, acc, bq,
                              stream));
-  // recompute the up projection's output (forward_qmm of _recompute_block)
-  QFFN_CUDA(qffn::launch_gemm_bf16(gu, yq, y_scale, w1, w1_scale, N, 2 * H, C, stream));
-  // swiglu_backward with the abs-max of d(gate|up)
-  QFFN_CUDA(qffn::launch_swiglu_backward(dgu, stats_dgu, dh, gu, N, H, stream));
+  // the up projection's output recomputed (forward_qmm of _recompute_block) and
+  // swiglu_backward with the abs-max of d(gate|up), in one GEMM epilogue
+  QFFN_CUDA(qffn::launch_gemm_swiglu_bwd(dgu, stats_dgu, dh, yq, y_scale, w1, w1_scale, N, H, C,
+                                         stream));
   // up projection: d_ln2, dW1
   return from_cuda(run_backward_qmm(d_ln2, dw1, stats_dgu, dgu, yq, y_scale, w1, w1_scale, N, C,
                                     2 * H, acc, bq, stream));

@@ -52,17 +52,6 @@ __global__ void __launch_bounds__(kThreads) transpose_u8_kernel(uint8_t* out, co
   }
 }
 
-// dg = dh * u * silu'(g), du = dh * silu(g) in fp32, each rounded once to bf16.
-// silu'(g) = s * (1 + g * (1 - s)) with s = sigmoid(g) formed from
-// e = exp(-|g|) in (0, 1], as in silu_mul_f32, so nothing overflows.
-QFFN_DEVI void swiglu_grad(float g, float u, float dh, float& dg, float& du) {
-  const float e = __expf(-fabsf(g));
-  const float r = __fdividef(1.0f, 1.0f + e);
-  const float s = g >= 0.0f ? r : e * r;
-  dg = (dh * u) * (s * (1.0f + g * (1.0f - s)));
-  du = dh * (g * s);
-}
-
 QFFN_DEVI float absmax8(uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
   float m = 0.0f;

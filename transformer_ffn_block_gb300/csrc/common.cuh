@@ -145,6 +145,17 @@ QFFN_DEVI float silu_mul_f32(float g, float u) {
   return (g * sig) * u;
 }
 
+// Gradient of silu(g) * u: dg = dh * u * silu'(g), du = dh * silu(g), in fp32
+// (each rounded once to bf16 by the caller).  silu'(g) = s * (1 + g * (1 - s))
+// with s = sigmoid(g) formed from e = exp(-|g|) as in silu_mul_f32.
+QFFN_DEVI void swiglu_grad(float g, float u, float dh, float& dg, float& du) {
+  const float e = __expf(-fabsf(g));
+  const float r = __fdividef(1.0f, 1.0f + e);
+  const float s = g >= 0.0f ? r : e * r;
+  dg = (dh * u) * (s * (1.0f + g * (1.0f - s)));
+  du = dh * (g * s);
+}
+
 // h = bf16(silu(g) * u) for the 8 bf16 pairs of two 16-byte vectors.
 QFFN_DEVI uint4 swiglu8(uint4 g, uint4 u) {
   const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};

@@ -6,6 +6,9 @@
 //                 [H,2H)); the tensor abs-max of h is recorded on the way.
 //   gemm_swiglu_quant : hq[M,H] = e4m3(h * 448 / amax_h) with amax_h given
 //                 (read from stats_h[0], not recorded); stats_h[1] = scale.
+//   gemm_swiglu_bwd : d_gu[M,2H] = (dh * u * silu'(g) | dh * silu(g)) for the
+//                 recomputed bf16 g, u and dh [M,H] read in the epilogue; the
+//                 abs-max of d_gu is recorded (recompute + swiglu_backward).
 //
 // These are the two matmuls of the FFN half of llmq "llama_model.cpp",
 // LLamaModel::_forward_block (forward_qmm -> matmul with weight and
@@ -94,6 +97,7 @@ __device__ unsigned int g_status;
 constexpr int EPI_BF16 = 0;          // out = bf16(scaled accumulator)
 constexpr int EPI_SWIGLU = 1;        // h = bf16(silu(g) * u), abs-max recorded
 constexpr int EPI_SWIGLU_E4M3 = 2;   // hq = e4m3(h * 448 / given abs-max)
+constexpr int EPI_SWIGLU_BWD = 3;    // d_gu = swiglu gradient from dh, abs-max recorded
 
 struct GemmArgs {
   void* out;
@@ -101,6 +105,7 @@ struct GemmArgs {
   const float* w_scale;
   float* amax;   // SwiGLU: stats_h {abs_max, scale}
   const uint16_t* bias;   // bf16 output: optional bf16 bias per output column
+  const uint16_t* dh;     // SwiGLU backward: gradient of h [M, H]
   int accumulate;         // bf16 output: add the previous contents of out (weight gradients)
   int M, N, K;   // N: output columns (SwiGLU: H)
   int H;         // SwiGLU: first up row of W1
@@ -446,6 +451,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t g[32], u[32];
           tmem_ld32x2(tbase + uint32_t(c0), tbase + uint32_t(128 + c0), g, u);
+          if (EPI == EPI_SWIGLU_BWD) {
+            // g, u rounded to bf16 as the recomputed gate|up buffer holds them,
+            // then the SwiGLU gradient with dh of the same row and columns
+            if (row_ok) {
+              const uint16_t* dhp = args.dh + hoff + c0;
+              uint32_t dw[16];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint4 d4 = ld16_ro(dhp + 8 * j);
+                dw[4 * j] = d4.x; dw[4 * j + 1] = d4.y; dw[4 * j + 2] = d4.z; dw[4 * j + 3] = d4.w;
+              }
+              uint32_t pg[16], pu[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float dg0, du0, dg1, du1;
+                swiglu_grad(round_bf16(__uint_as_float(g[2 * j]) * scale),
+                            round_bf16(__uint_as_float(u[2 * j]) * scale), bf16_lo(dw[j]), dg0, du0);
+                swiglu_grad(round_bf16(__uint_as_float(g[2 * j + 1]) * scale),
+                            round_bf16(__uint_as_float(u[2 * j + 1]) * scale), bf16_hi(dw[j]), dg1, du1);
+                pg[j] = pack_bf16x2(dg0, dg1);
+                pu[j] = pack_bf16x2(du0, du1);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(pg[j])), fabsf(bf16_hi(pg[j]))),
+                                         fmaxf(fabsf(bf16_lo(pu[j])), fabsf(bf16_hi(pu[j])))));
+              }
+              uint16_t* grow = static_cast<uint16_t*>(args.out) + size_t(row) * size_t(2 * args.N) +
+                               size_t(nb) * 128 + c0;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                stg16(grow + 8 * j, make_uint4(pg[4 * j], pg[4 * j + 1], pg[4 * j + 2], pg[4 * j + 3]));
+                stg16(grow + args.N + 8 * j,
+                      make_uint4(pu[4 * j], pu[4 * j + 1], pu[4 * j + 2], pu[4 * j + 3]));
+              }
+            }
+            continue;
+          }
           uint32_t p[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
@@ -482,7 +522,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
     }
-    if (EPI == EPI_SWIGLU) {
+    if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
       amax = warp_max(amax);
       if (lane == 0) atomic_max_nonneg(args.amax, amax);
     }
@@ -663,6 +703,20 @@ cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t*
   if (!swiglu_args(&a, &ma, &mb, hq, stats_h, A, a_scale, W1, w_scale, M, H, K))
     return cudaErrorInvalidValue;
   return launch<EPI_SWIGLU_E4M3>(ma, mb, a, s);
+}
+
+cudaError_t launch_gemm_swiglu_bwd(uint16_t* d_gu, float* stats, const uint16_t* dh,
+                                   const uint8_t* A, const float* a_scale, const uint8_t* W1,
+                                   const float* w_scale, int64_t M, int64_t H, int64_t K,
+                                   cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(stats, 0, sizeof(float), s);
+  if (e != cudaSuccess || M == 0) return e;
+  CUtensorMap ma, mb;
+  GemmArgs a;
+  if (!swiglu_args(&a, &ma, &mb, d_gu, stats, A, a_scale, W1, w_scale, M, H, K))
+    return cudaErrorInvalidValue;
+  a.dh = dh;
+  return launch<EPI_SWIGLU_BWD>(ma, mb, a, s);
 }
 
 cudaError_t gemm_take_status(unsigned int* status) {

@@ -49,6 +49,13 @@ cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, co
 cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* A,
                                      const float* a_scale, const uint8_t* W1, const float* w_scale,
                                      int64_t M, int64_t H, int64_t K, cudaStream_t s);
+// d_gu[M,2H] = SwiGLU gradient for dh [M,H] and the gate|up product of A and
+// W1 = [2H, K] (the recompute of gate_up fused with swiglu_backward); records
+// max|d_gu| into stats[0] (zeroed first).
+cudaError_t launch_gemm_swiglu_bwd(uint16_t* d_gu, float* stats, const uint16_t* dh,
+                                   const uint8_t* A, const float* a_scale, const uint8_t* W1,
+                                   const float* w_scale, int64_t M, int64_t H, int64_t K,
+                                   cudaStream_t s);
 // Reads and clears the GEMM kernels' device status word of the current device.
 cudaError_t gemm_take_status(unsigned int* status);
 
