@@ -515,6 +515,36 @@ def bench_backward(q, torch, device, steps, warmup, peaks):
     }
 
 
+def fp8_library_ceiling(torch, device, steps=10):
+    """Context only, not on the library's path: the FP8 rate of the vendor GEMM
+    (cuBLASLt through torch._scaled_mm, E4M3 x E4M3 -> bf16, per-tensor
+    scales) at 8192^3 and at the gate|up shape.  The roofline denominator stays
+    the measured bf16 peak x 2."""
+    res = {"what": "torch._scaled_mm (cuBLASLt) E4M3 GEMM, bf16 out, per-tensor scales"}
+    try:
+        g = torch.Generator(device="cpu").manual_seed(7)
+        one = torch.ones((), dtype=torch.float32, device=device)
+        for name, (m, n, k) in (("8192^3", (8192, 8192, 8192)), ("gate_up 16384x28672x4096", (16384, 28672, 4096))):
+            a = (torch.randn(m, k, generator=g) * 0.5).to(device).to(torch.float8_e4m3fn)
+            b = (torch.randn(n, k, generator=g) * 0.5).to(device).to(torch.float8_e4m3fn)
+            for _ in range(3):
+                torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / steps
+            res[name] = {"ms": ms, "tflops": 2.0 * m * n * k / (ms * 1e-3) / 1e12}
+            del a, b
+    except Exception as exc:          # reported, never fatal: this is context
+        res["unavailable"] = f"{type(exc).__name__}: {exc}"[:200]
+    return res
+
+
 def bench_decode(q, torch, device, iters, dist, peaks):
     cfg = DECODE_CFG
     C, H = cfg.C, cfg.H
@@ -761,6 +791,7 @@ def main():
     dec = bench_decode(q, torch, device, args.decode_iters, dist, peaks)
     att = bench_attention_projections(q, torch, device, args.steps, args.warmup)
     bwd = bench_backward(q, torch, device, max(3, args.steps // 4), args.warmup, peaks)
+    ceiling = fp8_library_ceiling(torch, device)
     cfg = PREFILL_CFG
     value = job_throughput(cfg.gemm_flop, world, pre["ms_per_step"])
     e2e_value = job_throughput(cfg.gemm_flop, world, pre["e2e_ms"])
@@ -783,6 +814,7 @@ def main():
         "recompute": pre["recompute"],
         "attention_projections": att,
         "backward": bwd,
+        "fp8_library_ceiling": ceiling,
         "decode": dec,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
