@@ -727,9 +727,10 @@ def run_reference(args, rank, world, dist):
 
 def profile_case(q, torch, device):
     """A case sized for ncu captures: the prefill chain at N=2048 tokens of the 8B FFN
-    (C=4096, H=14336; weights alone 176 MB, larger than L2; under 1 GB on the device)
-    three times, then the 8B decode FFN twice.  Launch order per forward: rmsnorm, quantize, gate|up GEMM,
-    quantize, down GEMM."""
+    (C=4096, H=14336; weights alone 176 MB, larger than L2; a few GB on the device at most)
+    three times, one recompute forward and one FP8 backward on the same tokens, then
+    the 8B decode FFN twice.  Launch order per forward: rmsnorm, quantize, gate|up
+    GEMM, quantize, down GEMM."""
     global PREFILL_CFG
     from ffn_inputs import PrefillConfig
     PREFILL_CFG = PrefillConfig("llama3-8b-2k", B=1, T=2048, C=4096, H=14336, eps=1e-5)
@@ -740,6 +741,29 @@ def profile_case(q, torch, device):
         forward(q, d, stream)
     torch.cuda.synchronize()
     q.qffn_check_status(stream)
+    # the recompute form and the FP8 backward on the same tokens (GEMM launches
+    # 6-7 and 8-12 of this process: recompute gate|up with the E4M3 epilogue and
+    # down; backward down dgrad, down wgrad, fused recompute + swiglu_backward,
+    # up dgrad, up wgrad)
+    pc = PREFILL_CFG
+    st_rec = d["stats"].clone()
+    q.qffn_forward_recompute(d["res_out"], d["out"], d["rstd"], st_rec[0:2], st_rec[2:4], d["res"],
+                             d["x"], d["gain"], pc.eps, d["w1"], d["w1_scale"], d["w2"], d["w2_scale"],
+                             pc.B, pc.T, pc.C, pc.H, d["ws"], stream=stream)
+    from ffn_inputs import random_bf16
+    dout = to_dev(random_bf16((pc.N, pc.C), seed=401, std=1e-3), torch, device)
+    bst = torch.zeros(4, dtype=torch.float32, device=device)
+    q.qffn_absmax(bst[0:2], dout, pc.N * pc.C, stream=stream)
+    d_ln2 = torch.empty(pc.N, pc.C, dtype=torch.int16, device=device)
+    dw1 = torch.empty(2 * pc.H, pc.C, dtype=torch.int16, device=device)
+    dw2 = torch.empty(pc.C, pc.H, dtype=torch.int16, device=device)
+    bws = torch.empty(q.qffn_ffn_backward_workspace_size(pc.N, pc.C, pc.H), dtype=torch.uint8, device=device)
+    q.qffn_ffn_backward(d_ln2, dw1, dw2, bst[0:2], bst[2:4], dout, d["yq"], d["stats"][1:2], d["hq"],
+                        d["stats"][3:4], d["w1"], d["w1_scale"], d["w2"], d["w2_scale"], pc.N, pc.C, pc.H,
+                        False, bws, stream=stream)
+    torch.cuda.synchronize()
+    q.qffn_check_status(stream)
+    del bws, d_ln2, dw1, dw2
     cfg = DECODE_CFG
     di = decode_inputs(cfg)
     recs = []
