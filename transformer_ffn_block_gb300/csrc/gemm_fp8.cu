@@ -79,7 +79,12 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
 constexpr int NUM_BARS = 2 * STAGES + 5;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + NUM_BARS * 8 + 16;
+// SwiGLU h staging for the TMA stores: 4 epilogue warps x 2 buffers of a
+// 32-row x 64-column bf16 box (4 KB, 128-byte swizzle)
+constexpr int STAGE_BOX_BYTES = 32 * 64 * 2;
+constexpr int STAGING_BYTES = 4 * 2 * STAGE_BOX_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + NUM_BARS * 8 + 16;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 constexpr int GROUP_M = 8;     // tile raster: 8 pair M-blocks (2048 rows) sweep the N-blocks together
 constexpr uint16_t kBothCtas = 0x3;
 constexpr uint16_t kLeaderOnly = 0x1;
@@ -192,6 +197,22 @@ QFFN_DEVI void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t b
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// 2-D tile store from shared memory (bulk-group completion); rows or columns
+// beyond the tensor's extent are not written.
+QFFN_DEVI void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+QFFN_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most one committed store group still reads shared memory.
+QFFN_DEVI void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Wait until every committed store group has completed.
+QFFN_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Order this thread's generic shared-memory writes before later async-proxy reads.
+QFFN_DEVI void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 QFFN_DEVI void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -264,13 +285,15 @@ QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
 template <int EPI, bool A_MN = false, bool B_MN = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmC,
                     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* sStaging = smem + STAGES * STAGE_BYTES;       // 1024-byte aligned
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sStaging + STAGING_BYTES);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
@@ -307,6 +330,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (EPI == EPI_SWIGLU) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -402,6 +426,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = int(rank) * BM + q * 32 + lane;
     const float scale = args.a_scale[0] * args.w_scale[0];
     float amax = 0.0f;
+    int sbuf = 0;            // EPI_SWIGLU: which of this warp's two staging boxes is next
     // EPI_SWIGLU_E4M3: quantise h with the given abs-max, as quantize_with_abs_max
     // does (fp32 product with 448 / abs_max, nearest even, saturating)
     float qinv = 0.0f;
@@ -451,7 +476,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else {
         const size_t hoff = size_t(row) * size_t(args.N) + size_t(nb) * 128;
-        uint16_t* hrow = static_cast<uint16_t*>(args.out) + hoff;
         uint8_t* qrow = static_cast<uint8_t*>(args.out) + hoff;
         // Eight columns of g and u per step in a rolled loop: the epilogue's
         // code stays small, so it does not crowd the producer's and the MMA
@@ -462,8 +486,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c0 = 0; c0 < 128; c0 += 8) {
           uint32_t g[8], u[8];
           tmem_ld8x2(tbase + uint32_t(c0), tbase + uint32_t(128 + c0), g, u);
-          if (!row_ok) continue;
           if (EPI == EPI_SWIGLU_BWD) {
+            if (!row_ok) continue;
             // g, u rounded to bf16 as the recomputed gate|up buffer holds them,
             // then the SwiGLU gradient with dh of the same row and columns
             const uint4 d4 = ld16_ro(args.dh + hoff + c0);
@@ -486,6 +510,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             stg16(grow, make_uint4(pg[0], pg[1], pg[2], pg[3]));
             stg16(grow + args.N, make_uint4(pu[0], pu[1], pu[2], pu[3]));
           } else {
+            // EPI_SWIGLU stages h in shared memory and stores it with TMA, one
+            // 32-row x 64-column box per warp and half tile: each lane writes
+            // its row's 16 bytes into the 128-byte-swizzled box (4 wavefronts
+            // per warp store), where per-thread 16-byte global stores would
+            // touch 32 rows per instruction.
+            uint8_t* sbox = sStaging + (q * 2 + sbuf) * STAGE_BOX_BYTES;
+            if (EPI == EPI_SWIGLU && (c0 & 63) == 0) {
+              if (lane == 0) bulk_wait_read_1();   // the store that last read this box is done
+              __syncwarp();
+            }
             uint32_t p[4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -494,10 +528,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float u0 = round_bf16(__uint_as_float(u[2 * j]) * scale);
               const float u1 = round_bf16(__uint_as_float(u[2 * j + 1]) * scale);
               p[j] = pack_bf16x2(silu_mul_f32(g0, u0), silu_mul_f32(g1, u1));
-              if (EPI == EPI_SWIGLU) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
+              if (EPI == EPI_SWIGLU && row_ok)
+                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
             }
-            if (EPI == EPI_SWIGLU) stg16(hrow + c0, make_uint4(p[0], p[1], p[2], p[3]));
-            if (EPI == EPI_SWIGLU_E4M3) {
+            if (EPI == EPI_SWIGLU) {
+              const int chunk = (c0 & 63) >> 3;
+              *reinterpret_cast<uint4*>(sbox + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
+                  make_uint4(p[0], p[1], p[2], p[3]);
+              if (chunk == 7) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
+                if (lane == 0) {
+                  if (row0 < args.M) tma_store_2d(&tmC, smem_u32(sbox), nb * 128 + (c0 & ~63), row0);
+                  bulk_commit();
+                }
+                sbuf ^= 1;
+              }
+            }
+            if (EPI == EPI_SWIGLU_E4M3 && row_ok) {
               uint32_t c[2];
 #pragma unroll
               for (int j = 0; j < 2; ++j) {
@@ -517,6 +566,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
     }
+    // the h stores complete (shared memory read, global memory written) before exit
+    if (EPI == EPI_SWIGLU && lane == 0) bulk_wait_all();
     if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
       amax = warp_max(amax);
       if (lane == 0) atomic_max_nonneg(args.amax, amax);
@@ -564,6 +615,20 @@ bool make_map(CUtensorMap* map, const uint8_t* ptr, int64_t rows, int64_t k) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor [rows, cols] (cols contiguous) as the target of the
+// epilogue's TMA stores: boxes of 32 rows x 64 columns, 128-byte swizzle.
+bool make_store_map_bf16(CUtensorMap* map, uint16_t* ptr, int64_t rows, int64_t cols) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  cuuint32_t box[2] = {64u, 32u};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Number of 2-CTA clusters of this kernel that fit on the device at once
 // (cached per device and form).
 template <int EPI, bool A_MN = false, bool B_MN = false>
@@ -600,7 +665,8 @@ cudaError_t max_pairs(int* pairs) {
 }
 
 template <int EPI, bool A_MN = false, bool B_MN = false>
-cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s) {
+cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s,
+                   const CUtensorMap* mc = nullptr) {
   int pairs = 0;
   cudaError_t e = max_pairs<EPI, A_MN, B_MN>(&pairs);
   if (e != cudaSuccess) return e;
@@ -617,7 +683,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, A_MN, B_MN>, ma, mb, a);
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, A_MN, B_MN>, ma, mb, mc != nullptr ? *mc : ma, a);
 }
 
 }  // namespace
@@ -685,7 +751,9 @@ cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, co
   GemmArgs a;
   if (!swiglu_args(&a, &ma, &mb, h, stats_h, A, a_scale, W1, w_scale, M, H, K))
     return cudaErrorInvalidValue;
-  return launch<EPI_SWIGLU>(ma, mb, a, s);
+  CUtensorMap mc;
+  if (!make_store_map_bf16(&mc, h, M, H)) return cudaErrorInvalidValue;
+  return launch<EPI_SWIGLU>(ma, mb, a, s, &mc);
 }
 
 cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* A,
