@@ -73,6 +73,24 @@ int qffn_abi_version(void);
  * check, QFFN_ERR_CUDA if the synchronisation failed, else QFFN_OK. */
 qffn_status qffn_check_status(qffn_stream_t stream);
 
+/* Self-test of the failure path (no counterpart on the pages, which stop on
+ * any CUDA error; this library bounds its device-side waits instead).  One
+ * CTA runs the GEMMs' bounded barrier wait on two barriers of arrival count 1:
+ * lane 0 of warp 0 waits up to `limit_ns` on barrier 0; lane 0 of warp 1 waits
+ * up to 4 x limit_ns on barrier 1 and leaves early if the CTA abort flag is
+ * raised.  With `arrive` != 0 both barriers get their arrival first and both
+ * waits succeed at once.  With arrive == 0 nothing arrives: warp 0 runs out,
+ * raises the abort flag and sets the device status word (the next
+ * qffn_check_status returns QFFN_ERR_TIMEOUT and clears it), and warp 1
+ * returns on the abort flag after about limit_ns.  Nothing faults or hangs and
+ * the context stays usable.
+ *   out: device, 4 x uint64, written by the kernel: out[0], out[1] = 1 if the
+ *        wait of warp 0 / warp 1 succeeded else 0; out[2], out[3] = the
+ *        nanoseconds (%globaltimer) each wait took.  8-byte aligned.
+ *   limit_ns: 100000 .. 2000000000 (QFFN_ERR_INVALID_ARG otherwise). */
+qffn_status qffn_selftest_bounded_wait(uint64_t* out, int arrive, int64_t limit_ns,
+                                       qffn_stream_t stream);
+
 /* ---- Step A1: fused residual add + RMSNorm + abs-max -----------------------
  * [llmq-model] fused_residual_rmsnorm_forward (and rmsnorm_forward when
  * res_in == NULL), called in _forward_block before the up projection.

@@ -184,3 +184,11 @@ def test_backward_checks(lib):
     assert f(A, A, A, A, A, A, A, A, 64, 256, 128, 0, A, ws - 1, None) == 1
     assert f(A, A, A, A, A, A, A, A, 64, 250, 128, 0, A, ws, None) == 2
     assert f(A, A, A, A, A, A, A, A, 64, 256, 128, 0, A + 16, ws, None) == 3
+
+
+def test_bounded_wait_selftest_argument_checks(lib):
+    f = lambda *a: _call(lib, "qffn_selftest_bounded_wait", *a)
+    assert f(NULL, 0, 1000000, None) == 1
+    assert f(A, 0, 99999, None) == 1                  # below 100 us
+    assert f(A, 0, 2000000001, None) == 1             # above 2 s
+    assert f(A + 4, 0, 1000000, None) == 3            # out not 8-byte aligned

@@ -3,6 +3,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/qffn.h"
 #include "launch.h"
 
@@ -17,6 +19,18 @@ inline bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) &
 inline size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 inline qffn_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QFFN_OK : QFFN_ERR_CUDA; }
+
+// An NVTX range named after the entry point around everything it enqueues, so
+// a timeline (Nsight Systems, ncu's NVTX filters) shows which call launched
+// which kernels.  Header-only NVTX: without an attached tool a push / pop is
+// a check of a function pointer.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define QFFN_RANGE() NvtxRange qffn_nvtx_range_(__func__)
 
 #define QFFN_REQUIRE(cond, err) \
   do {                          \
@@ -135,9 +149,20 @@ qffn_status qffn_check_status(qffn_stream_t stream) {
   return (st | sd) != 0 ? QFFN_ERR_TIMEOUT : QFFN_OK;
 }
 
+qffn_status qffn_selftest_bounded_wait(uint64_t* out, int arrive, int64_t limit_ns,
+                                       qffn_stream_t stream) {
+  QFFN_RANGE();
+  QFFN_PTR(out);
+  QFFN_REQUIRE(limit_ns >= 100000 && limit_ns <= 2000000000, QFFN_ERR_INVALID_ARG);
+  QFFN_REQUIRE(reinterpret_cast<uintptr_t>(out) % 8 == 0, QFFN_ERR_MISALIGNED);
+  return from_cuda(qffn::launch_wait_selftest(reinterpret_cast<unsigned long long*>(out),
+                                              arrive != 0, (unsigned long long)limit_ns, stream));
+}
+
 qffn_status qffn_rmsnorm_absmax(uint16_t* res_out, uint16_t* y, float* rstd, float* stats,
                                 const uint16_t* res_in, const uint16_t* x, const uint16_t* gain,
                                 float eps, int64_t N, int64_t C, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(y); QFFN_PTR(rstd); QFFN_PTR(x); QFFN_PTR(gain);
   if (res_in != nullptr) QFFN_PTR(res_out);
   QFFN_REQUIRE(N >= 0 && C >= 0, QFFN_ERR_INVALID_ARG);
@@ -152,6 +177,7 @@ qffn_status qffn_rmsnorm_absmax(uint16_t* res_out, uint16_t* y, float* rstd, flo
 }
 
 qffn_status qffn_absmax(float* stats, const uint16_t* in, int64_t n, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(stats); QFFN_PTR(in);
   QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_ALIGNED4(stats); QFFN_ALIGNED(in);
@@ -160,6 +186,7 @@ qffn_status qffn_absmax(float* stats, const uint16_t* in, int64_t n, qffn_stream
 
 qffn_status qffn_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t n,
                           qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(q); QFFN_PTR(stats); QFFN_PTR(in);
   QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_ALIGNED(q); QFFN_ALIGNED4(stats); QFFN_ALIGNED(in);
@@ -168,6 +195,7 @@ qffn_status qffn_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t 
 
 qffn_status qffn_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, int64_t rows,
                                int64_t cols, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(q); QFFN_PTR(row_scale); QFFN_PTR(w);
   QFFN_REQUIRE(rows >= 0 && cols >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(rows <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -179,6 +207,7 @@ qffn_status qffn_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, 
 qffn_status qffn_fp8_gemm_scaled(uint16_t* out, const uint8_t* A, const float* a_scale,
                                  const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
                                  int64_t K, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(A); QFFN_PTR(a_scale); QFFN_PTR(W); QFFN_PTR(w_scale);
   QFFN_REQUIRE(M >= 0 && N >= 0 && K >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(M <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -192,6 +221,7 @@ qffn_status qffn_fp8_gemm_scaled(uint16_t* out, const uint8_t* A, const float* a
 qffn_status qffn_qmm(uint16_t* out, uint8_t* q, float* stats, const uint16_t* in,
                      const uint16_t* bias, const uint8_t* W, const float* w_scale, int64_t M,
                      int64_t N, int64_t K, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(q); QFFN_PTR(stats); QFFN_PTR(in); QFFN_PTR(W); QFFN_PTR(w_scale);
   QFFN_REQUIRE(M >= 0 && N >= 0 && K >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(M <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -208,6 +238,7 @@ qffn_status qffn_qmm(uint16_t* out, uint8_t* q, float* stats, const uint16_t* in
 qffn_status qffn_gate_up_swiglu(uint16_t* h, float* stats_h, const uint8_t* yq,
                                 const float* y_scale, const uint8_t* w1, const float* w1_scale,
                                 int64_t N, int64_t C, int64_t H, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(h); QFFN_PTR(stats_h); QFFN_PTR(yq); QFFN_PTR(y_scale); QFFN_PTR(w1); QFFN_PTR(w1_scale);
   QFFN_REQUIRE(N >= 0 && C >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -221,6 +252,7 @@ qffn_status qffn_gate_up_swiglu(uint16_t* h, float* stats_h, const uint8_t* yq,
 
 qffn_status qffn_swiglu_quant(uint16_t* h, uint8_t* hq, float* stats, const uint16_t* gate_up,
                               int64_t N, int64_t H, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(hq); QFFN_PTR(stats); QFFN_PTR(gate_up);
   QFFN_REQUIRE(N >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(H % 8 == 0 && H >= 8 && H <= kMaxDim && N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -232,6 +264,7 @@ qffn_status qffn_swiglu_quant(uint16_t* h, uint8_t* hq, float* stats, const uint
 
 qffn_status qffn_swiglu_forward_quant(uint8_t* hq, float* stats, const uint16_t* gate_up,
                                       int64_t N, int64_t H, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(hq); QFFN_PTR(stats); QFFN_PTR(gate_up);
   QFFN_REQUIRE(N >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(H % 8 == 0 && H >= 8 && H <= kMaxDim && N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -243,6 +276,7 @@ qffn_status qffn_gate_up_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t
                                       const float* y_scale, const uint8_t* w1,
                                       const float* w1_scale, int64_t N, int64_t C, int64_t H,
                                       qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(hq); QFFN_PTR(stats_h); QFFN_PTR(yq); QFFN_PTR(y_scale); QFFN_PTR(w1); QFFN_PTR(w1_scale);
   QFFN_REQUIRE(N >= 0 && C >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -279,6 +313,7 @@ qffn_status qffn_forward(uint16_t* res_out, uint16_t* out, float* rstd, float* s
                          const float* w1_scale, const uint8_t* w2, const float* w2_scale,
                          int64_t B, int64_t T, int64_t C, int64_t H, void* workspace,
                          size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(rstd); QFFN_PTR(stats_y); QFFN_PTR(stats_h); QFFN_PTR(x);
   QFFN_PTR(gain); QFFN_PTR(w1); QFFN_PTR(w1_scale); QFFN_PTR(w2); QFFN_PTR(w2_scale);
   QFFN_PTR(workspace);
@@ -320,6 +355,7 @@ qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd
                                   const float* w1_scale, const uint8_t* w2, const float* w2_scale,
                                   int64_t B, int64_t T, int64_t C, int64_t H, void* workspace,
                                   size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(rstd); QFFN_PTR(stats_y); QFFN_PTR(stats_h); QFFN_PTR(x);
   QFFN_PTR(gain); QFFN_PTR(w1); QFFN_PTR(w1_scale); QFFN_PTR(w2); QFFN_PTR(w2_scale);
   QFFN_PTR(workspace);
@@ -354,6 +390,7 @@ qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd
 
 qffn_status qffn_transpose_e4m3(uint8_t* out, const uint8_t* in, int64_t rows, int64_t cols,
                                 qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(in);
   QFFN_REQUIRE(rows >= 0 && cols >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(rows % 16 == 0 && cols % 16 == 0 && rows <= kMaxRows && cols <= kMaxRows,
@@ -366,6 +403,7 @@ qffn_status qffn_transpose_e4m3(uint8_t* out, const uint8_t* in, int64_t rows, i
 qffn_status qffn_swiglu_backward(uint16_t* d_gate_up, float* stats, const uint16_t* dh,
                                  const uint16_t* gate_up, int64_t N, int64_t H,
                                  qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(d_gate_up); QFFN_PTR(stats); QFFN_PTR(dh); QFFN_PTR(gate_up);
   QFFN_REQUIRE(N >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(H % 8 == 0 && H >= 8 && H <= kMaxDim && N <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -385,6 +423,7 @@ qffn_status qffn_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout,
                               const uint8_t* w, const float* w_scale, int64_t N, int64_t IC,
                               int64_t OC, int accumulate, void* workspace, size_t workspace_bytes,
                               qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(dw); QFFN_PTR(stats_dout); QFFN_PTR(dout); QFFN_PTR(inp_q); QFFN_PTR(inp_scale);
   QFFN_PTR(w); QFFN_PTR(w_scale); QFFN_PTR(workspace);
   const qffn_status st = check_bqmm_shape(N, IC, OC);
@@ -419,6 +458,7 @@ qffn_status qffn_gate_up_swiglu_backward(uint16_t* d_gate_up, float* stats, cons
                                          const uint8_t* yq, const float* y_scale,
                                          const uint8_t* w1, const float* w1_scale, int64_t N,
                                          int64_t C, int64_t H, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(d_gate_up); QFFN_PTR(stats); QFFN_PTR(dh); QFFN_PTR(yq); QFFN_PTR(y_scale);
   QFFN_PTR(w1); QFFN_PTR(w1_scale);
   QFFN_REQUIRE(N >= 0 && C >= 0 && H >= 0, QFFN_ERR_INVALID_ARG);
@@ -438,6 +478,7 @@ qffn_status qffn_ffn_backward(uint16_t* d_ln2, uint16_t* dw1, uint16_t* dw2, flo
                               const uint8_t* w1, const float* w1_scale, const uint8_t* w2,
                               const float* w2_scale, int64_t N, int64_t C, int64_t H, int accumulate,
                               void* workspace, size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(d_ln2); QFFN_PTR(dw1); QFFN_PTR(dw2); QFFN_PTR(stats_dout); QFFN_PTR(stats_dgu);
   QFFN_PTR(dout); QFFN_PTR(yq); QFFN_PTR(y_scale); QFFN_PTR(hq); QFFN_PTR(h_scale);
   QFFN_PTR(w1); QFFN_PTR(w1_scale); QFFN_PTR(w2); QFFN_PTR(w2_scale); QFFN_PTR(workspace);
@@ -472,6 +513,7 @@ qffn_status qffn_ffn_backward(uint16_t* d_ln2, uint16_t* dw1, uint16_t* dw2, flo
 qffn_status qffn_gemv_dual(uint16_t* g, uint16_t* u, const uint16_t* x, const uint8_t* w_gate,
                            const float* s_gate, const uint8_t* w_up, const float* s_up,
                            int64_t H, int64_t C, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(g); QFFN_PTR(u); QFFN_PTR(x); QFFN_PTR(w_gate); QFFN_PTR(s_gate); QFFN_PTR(w_up); QFFN_PTR(s_up);
   QFFN_REQUIRE(H >= 1 && C >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(C % 16 == 0 && C >= 16 && C <= 32768 && H <= kMaxRows, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -481,6 +523,7 @@ qffn_status qffn_gemv_dual(uint16_t* g, uint16_t* u, const uint16_t* x, const ui
 
 qffn_status qffn_gemv(uint16_t* out, const uint16_t* x, const uint8_t* w, const float* row_scale,
                       int64_t rows, int64_t cols, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(x); QFFN_PTR(w); QFFN_PTR(row_scale);
   QFFN_REQUIRE(rows >= 1 && cols >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(cols % 16 == 0 && cols >= 16 && cols <= 32768 && rows <= kMaxRows,
@@ -493,6 +536,7 @@ qffn_status qffn_gemv(uint16_t* out, const uint16_t* x, const uint8_t* w, const 
 qffn_status qffn_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint16_t* u,
                                  const uint8_t* w, const float* row_scale, int64_t rows,
                                  int64_t cols, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(g); QFFN_PTR(u); QFFN_PTR(w); QFFN_PTR(row_scale);
   QFFN_REQUIRE(rows >= 1 && cols >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(cols % 16 == 0 && cols >= 16 && cols <= 32768 && rows <= kMaxRows,
@@ -502,6 +546,7 @@ qffn_status qffn_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint16_
 }
 
 qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(g); QFFN_PTR(u);
   QFFN_REQUIRE(n >= 0, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(n % 8 == 0, QFFN_ERR_UNSUPPORTED_SHAPE);
@@ -520,6 +565,7 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
                                 const float* s_gate, const uint8_t* w_up, const float* s_up,
                                 const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
                                 void* workspace, size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(x); QFFN_PTR(w_gate); QFFN_PTR(s_gate); QFFN_PTR(w_up); QFFN_PTR(s_up);
   QFFN_PTR(w_down); QFFN_PTR(s_down); QFFN_PTR(workspace);
   QFFN_REQUIRE(C % 16 == 0 && H % 16 == 0 && C >= 16 && H >= 16 && C <= 32768 && H <= 32768,

@@ -17,6 +17,8 @@
 // use the same array and race; order them on one stream or with events.
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/qffn.h"
 #include "launch.h"
 
@@ -58,11 +60,11 @@ inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3
 
 }  // namespace
 
-extern "C" qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t* x,
-                                                   const uint8_t* w_gate, const float* s_gate,
-                                                   const uint8_t* w_up, const float* s_up,
-                                                   const uint8_t* w_down, const float* s_down,
-                                                   int64_t C, int64_t H, qffn_stream_t stream) {
+static qffn_status decode_noalloc(uint16_t* out, const uint16_t* x,
+                                  const uint8_t* w_gate, const float* s_gate,
+                                  const uint8_t* w_up, const float* s_up,
+                                  const uint8_t* w_down, const float* s_down,
+                                  int64_t C, int64_t H, qffn_stream_t stream) {
   if (!out || !x || !w_gate || !s_gate || !w_up || !s_up || !w_down || !s_down)
     return QFFN_ERR_INVALID_ARG;
   if (C % 16 != 0 || H % 16 != 0 || C < 16 || H < 16 || C > kNoAllocMaxC || H > kNoAllocMaxH)
@@ -79,4 +81,16 @@ extern "C" qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t
       cudaSuccess)
     return QFFN_ERR_CUDA;
   return QFFN_OK;
+}
+
+extern "C" qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t* x,
+                                                   const uint8_t* w_gate, const float* s_gate,
+                                                   const uint8_t* w_up, const float* s_up,
+                                                   const uint8_t* w_down, const float* s_down,
+                                                   int64_t C, int64_t H, qffn_stream_t stream) {
+  nvtxRangePushA("qffn_decode_forward_noalloc");
+  const qffn_status st =
+      decode_noalloc(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, stream);
+  nvtxRangePop();
+  return st;
 }

@@ -33,7 +33,9 @@
 //   warps 2..5  epilogue (both CTAs): tcgen05.ld of the fp32 accumulator
 //               (one TMEM lane quarter per warp, one output row per thread,
 //               8 columns per step in a rolled loop), scaling, bf16 rounding,
-//               SwiGLU, abs-max, 16-byte stores; the
+//               SwiGLU, abs-max, 16-byte stores (h of the SwiGLU form:
+//               TMA stores of 32 x 64 boxes from a swizzled staging
+//               buffer, two per warp in flight); the
 //               accumulator is handed back to the leader's MMA thread by a
 //               remote mbarrier arrive.
 // Operands are K-major (K contiguous, "TN") by default.  The bf16 form also
@@ -780,6 +782,46 @@ cudaError_t launch_gemm_swiglu_bwd(uint16_t* d_gu, float* stats, const uint16_t*
     return cudaErrorInvalidValue;
   a.dh = dh;
   return launch<EPI_SWIGLU_BWD>(ma, mb, a, s);
+}
+
+// Self-test of the failure path: the bounded pipeline wait every GEMM role
+// uses, on two barriers of arrival count 1 in one CTA.  Lane 0 of warp 0
+// waits on barrier 0 for `limit` ns; lane 0 of warp 1 waits on barrier 1 for
+// 4 x limit and honours the CTA abort flag.  With `arrive` each barrier gets
+// its arrival first and both waits succeed at once.  Without it nothing
+// arrives: warp 0 runs out (abort flag up, g_status bit 0) and warp 1 leaves
+// on the abort flag, after about `limit` rather than its own 4 x limit.
+// out[0..1] = 1 if the wait of warp 0 / 1 succeeded, out[2..3] = its ns.
+__global__ void __launch_bounds__(64) wait_selftest_kernel(unsigned long long* out, int arrive,
+                                                           unsigned long long limit) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    mbar_init_fence();
+    if (arrive) {
+      mbar_arrive(smem_u32(&bars[0]));
+      mbar_arrive(smem_u32(&bars[1]));
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    const unsigned long long t0 = globaltimer();
+    const bool ok = mbar_wait(smem_u32(&bars[warp]), 0, abort_flag, true,
+                              warp == 0 ? limit : 4 * limit);
+    out[warp] = ok ? 1ull : 0ull;
+    out[2 + warp] = globaltimer() - t0;
+  }
+}
+
+cudaError_t launch_wait_selftest(unsigned long long* out, int arrive, unsigned long long limit_ns,
+                                 cudaStream_t s) {
+  wait_selftest_kernel<<<1, 64, 0, s>>>(out, arrive, limit_ns);
+  return cudaGetLastError();
 }
 
 cudaError_t gemm_take_status(unsigned int* status) {

@@ -58,6 +58,10 @@ cudaError_t launch_gemm_swiglu_bwd(uint16_t* d_gu, float* stats, const uint16_t*
                                    cudaStream_t s);
 // Reads and clears the GEMM kernels' device status word of the current device.
 cudaError_t gemm_take_status(unsigned int* status);
+// Failure-path self-test of the GEMMs' bounded barrier wait (one CTA, two
+// waits; out[4] as qffn_selftest_bounded_wait documents).
+cudaError_t launch_wait_selftest(unsigned long long* out, int arrive, unsigned long long limit_ns,
+                                 cudaStream_t s);
 
 // ---- FP8 backward (backward.cu)
 // out[Cc, R] = in[R, Cc]^T for E4M3 codes; R and Cc multiples of 16.
