@@ -273,7 +273,7 @@ def bench_prefill(q, torch, device, steps, warmup, dist, peaks):
         })
     s_in = torch.cuda.Stream(device)
     s_out = torch.cuda.Stream(device)
-    e_steps = max(4, min(steps, 12))
+    e_steps = max(4, steps)
 
     def e2e_step(i):
         b = bufs[i % 2]

@@ -337,16 +337,22 @@ qffn_status qffn_forward(uint16_t* res_out, uint16_t* out, float* rstd, float* s
   uint16_t* h = reinterpret_cast<uint16_t*>(ws + off[2]);
   uint8_t* hq = ws + off[3];
 
+  // The launches after A1 form a chain of programmatic dependent launches:
+  // each kernel is scheduled while its predecessor drains and waits for it
+  // to complete before touching global memory.  The stats_h[0] word is
+  // zeroed by A2's kernel instead of a memset, which would break the chain.
   // A1: r, y, rstd, stats_y[0]
   QFFN_CUDA(qffn::launch_rmsnorm(res_out, y, rstd, stats_y, res_in, x, gain, eps, N, int(C), stream));
-  // A2: yq, stats_y[1]
-  QFFN_CUDA(qffn::launch_quantize(yq, stats_y, y, N * C, stream));
+  // A2: yq, stats_y[1]; stats_h[0] = 0
+  QFFN_CUDA(qffn::launch_quantize(yq, stats_y, y, N * C, stream, true, stats_h));
   // A3 + A4: h, stats_h[0]
-  QFFN_CUDA(qffn::launch_gemm_swiglu(h, stats_h, yq, stats_y + 1, w1, w1_scale, N, H, C, stream));
+  QFFN_CUDA(qffn::launch_gemm_swiglu(h, stats_h, yq, stats_y + 1, w1, w1_scale, N, H, C, stream,
+                                     true));
   // A4 requantisation: hq, stats_h[1]
-  QFFN_CUDA(qffn::launch_quantize(hq, stats_h, h, N * H, stream));
+  QFFN_CUDA(qffn::launch_quantize(hq, stats_h, h, N * H, stream, true));
   // A5: out
-  return from_cuda(qffn::launch_gemm_bf16(out, hq, stats_h + 1, w2, w2_scale, N, C, H, stream));
+  return from_cuda(qffn::launch_gemm_bf16(out, hq, stats_h + 1, w2, w2_scale, N, C, H, stream,
+                                          nullptr, false, false, false, true));
 }
 
 qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd, float* stats_y,
@@ -380,12 +386,15 @@ qffn_status qffn_forward_recompute(uint16_t* res_out, uint16_t* out, float* rstd
 
   // A1 without recording an abs-max: r, y, rstd
   QFFN_CUDA(qffn::launch_rmsnorm(res_out, y, rstd, nullptr, res_in, x, gain, eps, N, int(C), stream));
+  // (the launches after A1 are chained as in qffn_forward)
   // A2 with the given abs-max of y: yq, stats_y[1]
-  QFFN_CUDA(qffn::launch_quantize(yq, stats_y, y, N * C, stream));
+  QFFN_CUDA(qffn::launch_quantize(yq, stats_y, y, N * C, stream, true));
   // A3 + A4 with the given abs-max of h: hq, stats_h[1] (bf16 h is never written)
-  QFFN_CUDA(qffn::launch_gemm_swiglu_quant(hq, stats_h, yq, stats_y + 1, w1, w1_scale, N, H, C, stream));
+  QFFN_CUDA(qffn::launch_gemm_swiglu_quant(hq, stats_h, yq, stats_y + 1, w1, w1_scale, N, H, C,
+                                           stream, true));
   // A5: out
-  return from_cuda(qffn::launch_gemm_bf16(out, hq, stats_h + 1, w2, w2_scale, N, C, H, stream));
+  return from_cuda(qffn::launch_gemm_bf16(out, hq, stats_h + 1, w2, w2_scale, N, C, H, stream,
+                                          nullptr, false, false, false, true));
 }
 
 qffn_status qffn_transpose_e4m3(uint8_t* out, const uint8_t* in, int64_t rows, int64_t cols,

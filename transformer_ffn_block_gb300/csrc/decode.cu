@@ -8,11 +8,15 @@
 // chunks t, t+TPR, ... of the row and issues all of its loads (16-byte,
 // non-allocating, one contiguous 16*TPR-byte span per load instruction)
 // before using any, so every thread keeps the whole row in flight.  x sits
-// in shared memory as bf16.  Products and sums are packed fp32x2 fmas: the
-// E4M3 pairs go through the e4m3x2 -> f16x2 convert to float pairs, x pairs
-// are widened from bf16 by shifts; even elements accumulate in the low half
-// and odd ones in the high half.  The per-row arithmetic (chunk order, pair
-// order, halves added, warp butterfly, warps of a team in order) is the same
+// in shared memory as bf16, the two 16-byte halves of each 32-byte chunk in
+// separate planes so that a warp's 16-byte reads are consecutive words (no
+// bank conflicts).  Products and sums are packed fp32x2 fmas: the E4M3 pairs
+// go through the e4m3x2 -> f16x2 convert to float pairs, x pairs are widened
+// from bf16 by shifts; even elements accumulate in the low half and odd ones
+// in the high half.  (Staging x widened to fp32 instead was measured slower:
+// twice the shared-memory reads for the same work.)  The per-row arithmetic
+// (chunk order, pair order, halves added, warp butterfly, warps of a team in
+// order) is the same
 // code for the single and the dual form, so they agree bit for bit; the dual
 // form reads x once for the gate and the up row of the same index.
 //
@@ -37,6 +41,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kUSingle = 8;                // 16-byte loads in flight per thread
 constexpr int kUDual = 4;                  //   (per matrix)
+constexpr int kXU = 4;                     // input-vector loads in flight per thread
 
 QFFN_DEVI uint64_t e4m3x2_to_f2(uint32_t two_codes) {
   uint32_t h;
@@ -104,9 +109,32 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
   }
   pdl_wait();                        // x may come from the preceding kernel
   pdl_trigger();
-  for (int i = threadIdx.x; i < nvec; i += kThreads)
-    xs[i] = SILU_IN ? swiglu8(ld16_once(G.x + size_t(i) * 8), ld16_once(G.x_up + size_t(i) * 8))
-                    : ld16_once(G.x + size_t(i) * 8);
+  // Stage x: a thread issues up to kXU of its 16-byte loads before its first
+  // shared-memory store, so staging costs one L2 round trip per kXU vectors
+  // rather than one per vector (7 per thread for a 14336-long input).
+  constexpr int kX = SILU_IN ? 2 : kXU;   // SiLU staging holds two vectors per load
+  for (int i0 = threadIdx.x; i0 < nvec; i0 += kThreads * kX) {
+    uint4 v[kX], vu[kX];
+#pragma unroll
+    for (int j = 0; j < kX; ++j) {
+      const int i = i0 + j * kThreads;
+      if (i < nvec) {
+        v[j] = ld16_once(G.x + size_t(i) * 8);
+        if constexpr (SILU_IN) vu[j] = ld16_once(G.x_up + size_t(i) * 8);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kX; ++j) {
+      const int i = i0 + j * kThreads;
+      if (i < nvec) {
+        // part-major layout: part p of chunk c at xs[p * nchunk + c], so the
+        // lanes of a warp (consecutive chunks) read consecutive 16-byte words
+        const int c = i >> 1, h = i & 1;
+        if constexpr (SILU_IN) xs[h * nchunk + c] = swiglu8(v[j], vu[j]);
+        else xs[h * nchunk + c] = v[j];
+      }
+    }
+  }
   __syncthreads();
 
   for (int base = blockIdx.x * RPB; base < rows; base += gridDim.x * RPB) {
@@ -131,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
         for (int u = 0; u < kU; ++u) {
           const int cc = c + TPR * u;
           if (cc < nchunk) {
-            const uint4 xa = xs[2 * cc], xb = xs[2 * cc + 1];
+            const uint4 xa = xs[cc], xb = xs[nchunk + cc];
             dot16(a[u], xa, xb, acc0);
             if (DUAL) dot16(b[u], xa, xb, acc1);
           }

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(128) rmsnorm_kernel(uint16_t* res_out, uint16_
                                                       float eps, int C) {
   __shared__ float red[8];
   __shared__ float s_rstd[2];
+  pdl_trigger();                     // lets the next kernel of a chain be scheduled
   const int64_t row = blockIdx.x;
   const int nchunk = C >> 3;
   const int tid = threadIdx.x;
@@ -192,7 +193,11 @@ __global__ void __launch_bounds__(kThreads) absmax_kernel(float* stats, const ui
 // ------------------------------------------------------------------ A2
 // 16 elements per thread per step: two 16-byte loads, one 16-byte store.
 __global__ void __launch_bounds__(kThreads) quantize_kernel(uint8_t* q, float* stats,
-                                                            const uint16_t* in, int64_t n) {
+                                                            const uint16_t* in, int64_t n,
+                                                            float* zero_stat) {
+  pdl_wait();                        // in a chain: the preceding kernel has completed
+  pdl_trigger();
+  if (zero_stat != nullptr && blockIdx.x == 0 && threadIdx.x == 0) *zero_stat = 0.0f;
   const float amax = stats[0];
   const bool zero = !(amax > 0.0f);
   const float inv = zero ? 0.0f : 448.0f / amax;
@@ -391,9 +396,17 @@ cudaError_t launch_absmax(float* stats, const uint16_t* in, int64_t n, cudaStrea
 }
 
 cudaError_t launch_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t n,
-                            cudaStream_t s) {
-  quantize_kernel<<<grid_for(n / 16 + 1, 8), kThreads, 0, s>>>(q, stats, in, n);
-  return cudaGetLastError();
+                            cudaStream_t s, bool pdl, float* zero_stat) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_for(n / 16 + 1, 8));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, quantize_kernel, q, stats, in, n, zero_stat);
 }
 
 cudaError_t launch_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, int64_t rows,

@@ -346,6 +346,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent launch in the forward chains: the
+  // set-up above overlaps the preceding kernel's tail; nothing in global
+  // memory is read or written before the preceding kernel has completed.
+  // (Both are no-ops in a plain launch.)
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -668,7 +674,7 @@ cudaError_t max_pairs(int* pairs) {
 
 template <int EPI, bool A_MN = false, bool B_MN = false>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s,
-                   const CUtensorMap* mc = nullptr) {
+                   const CUtensorMap* mc = nullptr, bool pdl = false) {
   int pairs = 0;
   cudaError_t e = max_pairs<EPI, A_MN, B_MN>(&pairs);
   if (e != cudaSuccess) return e;
@@ -678,13 +684,15 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, A_MN, B_MN>, ma, mb, mc != nullptr ? *mc : ma, a);
 }
 
@@ -693,7 +701,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
 cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
                              const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
                              int64_t K, cudaStream_t s, const uint16_t* bias, bool accumulate,
-                             bool a_mn, bool w_mn) {
+                             bool a_mn, bool w_mn, bool pdl) {
   if (M == 0) return cudaSuccess;
   CUtensorMap ma, mb;
   // an MN-major operand lies in memory as [K rows, M (N) contiguous]
@@ -715,10 +723,10 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.tiles_n = int((N + BN - 1) / BN);
   a.num_tiles = a.tiles_m * a.tiles_n;
   a.num_kb = int((K + KBOX * BK - 1) / (KBOX * BK));
-  if (a_mn && w_mn) return launch<EPI_BF16, true, true>(ma, mb, a, s);
-  if (a_mn) return launch<EPI_BF16, true, false>(ma, mb, a, s);
-  if (w_mn) return launch<EPI_BF16, false, true>(ma, mb, a, s);
-  return launch<EPI_BF16>(ma, mb, a, s);
+  if (a_mn && w_mn) return launch<EPI_BF16, true, true>(ma, mb, a, s, nullptr, pdl);
+  if (a_mn) return launch<EPI_BF16, true, false>(ma, mb, a, s, nullptr, pdl);
+  if (w_mn) return launch<EPI_BF16, false, true>(ma, mb, a, s, nullptr, pdl);
+  return launch<EPI_BF16>(ma, mb, a, s, nullptr, pdl);
 }
 
 namespace {
@@ -746,28 +754,32 @@ bool swiglu_args(GemmArgs* a, CUtensorMap* ma, CUtensorMap* mb, void* out, float
 
 cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, const float* a_scale,
                                const uint8_t* W1, const float* w_scale, int64_t M, int64_t H,
-                               int64_t K, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(stats_h, 0, sizeof(float), s);
-  if (e != cudaSuccess || M == 0) return e;
+                               int64_t K, cudaStream_t s, bool chained) {
+  if (!chained) {
+    cudaError_t e = cudaMemsetAsync(stats_h, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+  }
+  if (M == 0) return cudaSuccess;
   CUtensorMap ma, mb;
   GemmArgs a;
   if (!swiglu_args(&a, &ma, &mb, h, stats_h, A, a_scale, W1, w_scale, M, H, K))
     return cudaErrorInvalidValue;
   CUtensorMap mc;
   if (!make_store_map_bf16(&mc, h, M, H)) return cudaErrorInvalidValue;
-  return launch<EPI_SWIGLU>(ma, mb, a, s, &mc);
+  return launch<EPI_SWIGLU>(ma, mb, a, s, &mc, chained);
 }
 
 cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* A,
                                      const float* a_scale, const uint8_t* W1, const float* w_scale,
-                                     int64_t M, int64_t H, int64_t K, cudaStream_t s) {
+                                     int64_t M, int64_t H, int64_t K, cudaStream_t s,
+                                     bool pdl) {
   // no rows: only the scale word is written (the elementwise form with N = 0)
   if (M == 0) return launch_swiglu_requant(hq, stats_h, nullptr, 0, H, s);
   CUtensorMap ma, mb;
   GemmArgs a;
   if (!swiglu_args(&a, &ma, &mb, hq, stats_h, A, a_scale, W1, w_scale, M, H, K))
     return cudaErrorInvalidValue;
-  return launch<EPI_SWIGLU_E4M3>(ma, mb, a, s);
+  return launch<EPI_SWIGLU_E4M3>(ma, mb, a, s, nullptr, pdl);
 }
 
 cudaError_t launch_gemm_swiglu_bwd(uint16_t* d_gu, float* stats, const uint16_t* dh,

@@ -16,8 +16,13 @@ cudaError_t launch_rmsnorm(uint16_t* res_out, uint16_t* y, float* rstd, float* s
                            const uint16_t* res_in, const uint16_t* x, const uint16_t* gain,
                            float eps, int64_t N, int C, cudaStream_t s);
 cudaError_t launch_absmax(float* stats, const uint16_t* in, int64_t n, cudaStream_t s);
+// Chained launches (pdl): the kernel is a programmatic dependent launch; it
+// waits for the preceding kernel on `s` before touching global memory.
+// zero_stat (optional): set to 0 by the kernel once that wait is over, so a
+// later kernel of the same chain can record an abs-max there without a
+// memset (which would break the chain).
 cudaError_t launch_quantize(uint8_t* q, float* stats, const uint16_t* in, int64_t n,
-                            cudaStream_t s);
+                            cudaStream_t s, bool pdl = false, float* zero_stat = nullptr);
 cudaError_t launch_quantize_rows(uint8_t* q, float* row_scale, const uint16_t* w, int64_t rows,
                                  int cols, cudaStream_t s);
 // SwiGLU over gate_up [N, 2H]: writes h (if non-NULL) and max|h| into stats[0]
@@ -38,17 +43,21 @@ cudaError_t launch_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, bool pdl,
 cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
                              const uint8_t* W, const float* w_scale, int64_t M, int64_t N,
                              int64_t K, cudaStream_t s, const uint16_t* bias = nullptr,
-                             bool accumulate = false, bool a_mn = false, bool w_mn = false);
+                             bool accumulate = false, bool a_mn = false, bool w_mn = false,
+                             bool pdl = false);
 // h[M,H] = bf16(silu(g)*u) with g, u the bf16-rounded gate / up products of
-// W1 = [2H, K]; records max|h| into stats_h[0] (zeroed first).
+// W1 = [2H, K]; records max|h| into stats_h[0] (zeroed first by a memset,
+// or, with `chained`, already zeroed by an earlier kernel of the chain: the
+// GEMM is then a programmatic dependent launch).
 cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, const float* a_scale,
                                const uint8_t* W1, const float* w_scale, int64_t M, int64_t H,
-                               int64_t K, cudaStream_t s);
+                               int64_t K, cudaStream_t s, bool chained = false);
 // hq[M,H] = e4m3(h * 448 / stats_h[0]) for the h of launch_gemm_swiglu, with
 // the abs-max given (not recorded); writes stats_h[1] = scale.
 cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* A,
                                      const float* a_scale, const uint8_t* W1, const float* w_scale,
-                                     int64_t M, int64_t H, int64_t K, cudaStream_t s);
+                                     int64_t M, int64_t H, int64_t K, cudaStream_t s,
+                                     bool pdl = false);
 // d_gu[M,2H] = SwiGLU gradient for dh [M,H] and the gate|up product of A and
 // W1 = [2H, K] (the recompute of gate_up fused with swiglu_backward); records
 // max|d_gu| into stats[0] (zeroed first).
