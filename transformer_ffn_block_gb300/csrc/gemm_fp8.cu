@@ -254,14 +254,14 @@ QFFN_DEVI void mma_commit_mc(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 
-// Eight 32-bit TMEM columns at each of two addresses (this warp's lane
-// quarter), one wait for both.
 // Eight 32-bit TMEM columns of this warp's lane quarter.
 QFFN_DEVI void tmem_ld8(uint32_t taddr, uint32_t (&v)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                "tcgen05.wait::ld.sync.aligned;\n"
                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]) : "r"(taddr) : "memory");
 }
+// Eight 32-bit TMEM columns at each of two addresses (this warp's lane
+// quarter), one wait for both.
 QFFN_DEVI void tmem_ld8x2(uint32_t ta, uint32_t tb, uint32_t (&a)[8], uint32_t (&b)[8]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n"
