@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI == EPI_SWIGLU) tma_prefetch_desc(&tmC);
+    if (EPI == EPI_SWIGLU || (EPI == EPI_BF16 && !args.accumulate)) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = int(rank) * BM + q * 32 + lane;
     const float scale = args.a_scale[0] * args.w_scale[0];
     float amax = 0.0f;
-    int sbuf = 0;            // EPI_SWIGLU: which of this warp's two staging boxes is next
+    int sbuf = 0;            // TMA-store forms: which of this warp's two staging boxes is next
     // EPI_SWIGLU_E4M3: quantise h with the given abs-max, as quantize_with_abs_max
     // does (fp32 product with 448 / abs_max, nearest even, saturating)
     float qinv = 0.0f;
@@ -456,7 +456,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = mb * (2 * BM) + row_in_tile;
       const bool row_ok = row < args.M;
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
-      if (!SWIGLU) {
+      if (!SWIGLU && !args.accumulate) {
+        // bf16 out staged in shared memory and stored with TMA, one 32-row x
+        // 64-column box per warp at a time (two buffers), as h in the SwiGLU
+        // form: a warp's per-row 16-byte global stores would touch 32 rows
+        // per instruction and load the L1 data pipe that the tensor core's
+        // shared-memory operand reads also use.  The tensor map clips rows
+        // beyond M and columns beyond N.
+        const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 8) {
+          uint32_t v[8];
+          tmem_ld8(tbase + uint32_t(c0), v);
+          const int col = nb * BN + c0;
+          const int chunk = (c0 & 63) >> 3;
+          uint8_t* sbox = sStaging + (q * 2 + sbuf) * STAGE_BOX_BYTES;
+          if (chunk == 0) {
+            if (lane == 0) bulk_wait_read_1();   // the store that last read this box is done
+            __syncwarp();
+          }
+          uint32_t p[4];
+          if (args.bias != nullptr) {
+            const uint4 b4 = col < args.N ? ld16_ro(args.bias + col) : make_uint4(0, 0, 0, 0);
+            const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              p[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * scale + bf16_lo(bw[j]),
+                                 __uint_as_float(v[2 * j + 1]) * scale + bf16_hi(bw[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              p[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * scale, __uint_as_float(v[2 * j + 1]) * scale);
+          }
+          *reinterpret_cast<uint4*>(sbox + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
+              make_uint4(p[0], p[1], p[2], p[3]);
+          if (chunk == 7) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            const int x = nb * BN + (c0 & ~63);
+            if (lane == 0) {
+              if (row0 < args.M && x < args.N) tma_store_2d(&tmC, smem_u32(sbox), x, row0);
+              bulk_commit();
+            }
+            sbuf ^= 1;
+          }
+        }
+      } else if (!SWIGLU) {
+        // accumulating form (weight gradients): read-modify-write per row
         uint16_t* orow = static_cast<uint16_t*>(args.out) + size_t(row) * size_t(args.N);
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 8) {
@@ -574,8 +620,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
     }
-    // the h stores complete (shared memory read, global memory written) before exit
-    if (EPI == EPI_SWIGLU && lane == 0) bulk_wait_all();
+    // the TMA stores complete (shared memory read, global memory written) before exit
+    if ((EPI == EPI_SWIGLU || (EPI == EPI_BF16 && !args.accumulate)) && lane == 0) bulk_wait_all();
     if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
       amax = warp_max(amax);
       if (lane == 0) atomic_max_nonneg(args.amax, amax);
@@ -723,10 +769,17 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.tiles_n = int((N + BN - 1) / BN);
   a.num_tiles = a.tiles_m * a.tiles_n;
   a.num_kb = int((K + KBOX * BK - 1) / (KBOX * BK));
-  if (a_mn && w_mn) return launch<EPI_BF16, true, true>(ma, mb, a, s, nullptr, pdl);
-  if (a_mn) return launch<EPI_BF16, true, false>(ma, mb, a, s, nullptr, pdl);
-  if (w_mn) return launch<EPI_BF16, false, true>(ma, mb, a, s, nullptr, pdl);
-  return launch<EPI_BF16>(ma, mb, a, s, nullptr, pdl);
+  // the output tensor map of the TMA-store epilogue (not used when accumulating)
+  CUtensorMap mc;
+  const CUtensorMap* pmc = nullptr;
+  if (!accumulate) {
+    if (!make_store_map_bf16(&mc, out, M, N)) return cudaErrorInvalidValue;
+    pmc = &mc;
+  }
+  if (a_mn && w_mn) return launch<EPI_BF16, true, true>(ma, mb, a, s, pmc, pdl);
+  if (a_mn) return launch<EPI_BF16, true, false>(ma, mb, a, s, pmc, pdl);
+  if (w_mn) return launch<EPI_BF16, false, true>(ma, mb, a, s, pmc, pdl);
+  return launch<EPI_BF16>(ma, mb, a, s, pmc, pdl);
 }
 
 namespace {
