@@ -80,7 +80,7 @@ constexpr int B_BYTES = KBOX * BOX_BYTES;  // this CTA's half of the B rows of a
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int NUM_BARS = 2 * STAGES + 5;
+constexpr int NUM_BARS = 2 * STAGES + 5 + 4;   // + one per epilogue warp (SwiGLU backward's dh loads)
 // SwiGLU h staging for the TMA stores: 4 epilogue warps x 2 buffers of a
 // 32-row x 64-column bf16 box (4 KB, 128-byte swizzle)
 constexpr int STAGE_BOX_BYTES = 32 * 64 * 2;
@@ -199,6 +199,15 @@ QFFN_DEVI void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t b
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// 2-D tile load into this CTA's shared memory, completing on its barrier `bar`;
+// elements outside the tensor are filled with zeros.
+QFFN_DEVI void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
 // 2-D tile store from shared memory (bulk-group completion); rows or columns
 // beyond the tensor's extent are not written.
 QFFN_DEVI void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
@@ -210,6 +219,8 @@ QFFN_DEVI void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) 
 QFFN_DEVI void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most one committed store group still reads shared memory.
 QFFN_DEVI void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Wait until no committed store group still reads shared memory.
+QFFN_DEVI void bulk_wait_read_0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Wait until every committed store group has completed.
 QFFN_DEVI void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Order this thread's generic shared-memory writes before later async-proxy reads.
@@ -288,6 +299,7 @@ template <int EPI, bool A_MN = false, bool B_MN = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC,
+                    const __grid_constant__ CUtensorMap tmD,
                     const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -310,6 +322,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 4);
+  //   dh[q]      epilogue warp of lane quarter q: its dh box has landed (SwiGLU backward)
+  auto dh_bar = [&](int q) { return bar0 + 8u * uint32_t(2 * STAGES + 5 + q); };
 
   constexpr bool SWIGLU = EPI != EPI_BF16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -326,13 +340,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(tempty_bar(a), 8);
     }
     mbar_init(drain_bar, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(dh_bar(q), 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI == EPI_SWIGLU || (EPI == EPI_BF16 && !args.accumulate)) tma_prefetch_desc(&tmC);
+    if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || (EPI == EPI_BF16 && !args.accumulate))
+      tma_prefetch_desc(&tmC);
+    if (EPI == EPI_SWIGLU_BWD) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -445,6 +462,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       qinv = qzero ? 0.0f : 448.0f / given;
       if (blockIdx.x == 0 && threadIdx.x == 64) args.amax[1] = qzero ? 1.0f : given / 448.0f;
     }
+    // EPI_SWIGLU_BWD: dh comes in by TMA, one 32-row x 64-column box per warp
+    // and half tile, into staging box A of the warp; dg is written back over
+    // it and du into box B, and both go out by TMA stores.  The first half's
+    // box of the next tile is requested as soon as this tile's stores have
+    // read the boxes, so it lands while the next accumulator is computed.
+    uint8_t* boxA = sStaging + (q * 2) * STAGE_BOX_BYTES;
+    uint8_t* boxB = boxA + STAGE_BOX_BYTES;
+    uint32_t dh_par = 0;
+    bool dh_pending = false;   // lane 0: a dh load has been issued and not waited for
+    auto load_dh = [&](int t, int half) {    // lane 0
+      int pmb, pnb;
+      tile_coords(t, args, pmb, pnb);
+      const int prow0 = pmb * (2 * BM) + int(rank) * BM + q * 32;
+      mbar_expect_tx(dh_bar(q), STAGE_BOX_BYTES);
+      tma_load_2d(smem_u32(boxA), &tmD, dh_bar(q), pnb * 128 + half * 64, prow0);
+      dh_pending = true;
+    };
+    if (EPI == EPI_SWIGLU_BWD && lane == 0 && pair < args.num_tiles) load_dh(pair, 0);
     int local = 0;
     for (int tile = pair; tile < args.num_tiles; tile += num_pairs, ++local) {
       const int acc = local & 1;
@@ -528,6 +563,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             stg16(orow + col, make_uint4(p[0], p[1], p[2], p[3]));
           }
         }
+      } else if (EPI == EPI_SWIGLU_BWD) {
+        const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
+        bool ok = true;
+        for (int half = 0; half < 2; ++half) {
+          if (half == 1) {
+            if (lane == 0) {
+              bulk_wait_read_0();              // half 0's stores have read both boxes
+              load_dh(tile, 1);
+            }
+            __syncwarp();
+          }
+          if (!mbar_wait(dh_bar(q), dh_par, abort_flag)) { ok = false; break; }
+          dh_par ^= 1u;
+          if (lane == 0) dh_pending = false;
+#pragma unroll 1
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const int c0 = half * 64 + c8 * 8;
+            uint32_t g[8], u[8];
+            tmem_ld8x2(tbase + uint32_t(c0), tbase + uint32_t(128 + c0), g, u);
+            // this lane's row, 16-byte chunk c8 of the 128-byte-swizzled boxes
+            const uint32_t off = uint32_t(lane) * 128u + (uint32_t(c8 ^ (lane & 7)) << 4);
+            const uint4 d4 = *reinterpret_cast<const uint4*>(boxA + off);
+            const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
+            uint32_t pg[4], pu[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              // g, u rounded to bf16 as the recomputed gate|up buffer holds them,
+              // then the SwiGLU gradient with dh of the same row and columns
+              float dg0, du0, dg1, du1;
+              swiglu_grad(round_bf16(__uint_as_float(g[2 * j]) * scale),
+                          round_bf16(__uint_as_float(u[2 * j]) * scale), bf16_lo(dw[j]), dg0, du0);
+              swiglu_grad(round_bf16(__uint_as_float(g[2 * j + 1]) * scale),
+                          round_bf16(__uint_as_float(u[2 * j + 1]) * scale), bf16_hi(dw[j]), dg1, du1);
+              pg[j] = pack_bf16x2(dg0, dg1);
+              pu[j] = pack_bf16x2(du0, du1);
+              if (row_ok)
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(pg[j])), fabsf(bf16_hi(pg[j]))),
+                                         fmaxf(fabsf(bf16_lo(pu[j])), fabsf(bf16_hi(pu[j])))));
+            }
+            *reinterpret_cast<uint4*>(boxA + off) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+            *reinterpret_cast<uint4*>(boxB + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            // rows beyond M are clipped by the tensor map
+            if (row0 < args.M) {
+              tma_store_2d(&tmC, smem_u32(boxA), nb * 128 + half * 64, row0);
+              tma_store_2d(&tmC, smem_u32(boxB), args.N + nb * 128 + half * 64, row0);
+            }
+            bulk_commit();
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) {
+          bulk_wait_read_0();                  // the stores have read box A
+          if (tile + num_pairs < args.num_tiles) load_dh(tile + num_pairs, 0);
+        }
+        __syncwarp();
       } else {
         const size_t hoff = size_t(row) * size_t(args.N) + size_t(nb) * 128;
         uint8_t* qrow = static_cast<uint8_t*>(args.out) + hoff;
@@ -540,30 +634,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int c0 = 0; c0 < 128; c0 += 8) {
           uint32_t g[8], u[8];
           tmem_ld8x2(tbase + uint32_t(c0), tbase + uint32_t(128 + c0), g, u);
-          if (EPI == EPI_SWIGLU_BWD) {
-            if (!row_ok) continue;
-            // g, u rounded to bf16 as the recomputed gate|up buffer holds them,
-            // then the SwiGLU gradient with dh of the same row and columns
-            const uint4 d4 = ld16_ro(args.dh + hoff + c0);
-            const uint32_t dw[4] = {d4.x, d4.y, d4.z, d4.w};
-            uint32_t pg[4], pu[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              float dg0, du0, dg1, du1;
-              swiglu_grad(round_bf16(__uint_as_float(g[2 * j]) * scale),
-                          round_bf16(__uint_as_float(u[2 * j]) * scale), bf16_lo(dw[j]), dg0, du0);
-              swiglu_grad(round_bf16(__uint_as_float(g[2 * j + 1]) * scale),
-                          round_bf16(__uint_as_float(u[2 * j + 1]) * scale), bf16_hi(dw[j]), dg1, du1);
-              pg[j] = pack_bf16x2(dg0, dg1);
-              pu[j] = pack_bf16x2(du0, du1);
-              amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo(pg[j])), fabsf(bf16_hi(pg[j]))),
-                                       fmaxf(fabsf(bf16_lo(pu[j])), fabsf(bf16_hi(pu[j])))));
-            }
-            uint16_t* grow = static_cast<uint16_t*>(args.out) + size_t(row) * size_t(2 * args.N) +
-                             size_t(nb) * 128 + c0;
-            stg16(grow, make_uint4(pg[0], pg[1], pg[2], pg[3]));
-            stg16(grow + args.N, make_uint4(pu[0], pu[1], pu[2], pu[3]));
-          } else {
+          {
             // EPI_SWIGLU stages h in shared memory and stores it with TMA, one
             // 32-row x 64-column box per warp and half tile: each lane writes
             // its row's 16 bytes into the 128-byte-swizzled box (4 wavefronts
@@ -620,8 +691,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(map_to_rank(tempty_bar(acc), 0));
     }
-    // the TMA stores complete (shared memory read, global memory written) before exit
-    if ((EPI == EPI_SWIGLU || (EPI == EPI_BF16 && !args.accumulate)) && lane == 0) bulk_wait_all();
+    // the TMA stores complete (shared memory read, global memory written) and
+    // no TMA load into shared memory is in flight before exit
+    if ((EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || (EPI == EPI_BF16 && !args.accumulate)) &&
+        lane == 0)
+      bulk_wait_all();
+    if (EPI == EPI_SWIGLU_BWD && lane == 0 && dh_pending)
+      mbar_wait(dh_bar(q), dh_par, abort_flag, false, kDrainLimitNs);
     if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
       amax = warp_max(amax);
       if (lane == 0) atomic_max_nonneg(args.amax, amax);
@@ -669,8 +745,9 @@ bool make_map(CUtensorMap* map, const uint8_t* ptr, int64_t rows, int64_t k) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D bf16 tensor [rows, cols] (cols contiguous) as the target of the
-// epilogue's TMA stores: boxes of 32 rows x 64 columns, 128-byte swizzle.
+// 2-D bf16 tensor [rows, cols] (cols contiguous) for the epilogue's TMA
+// stores (and the SwiGLU backward's dh loads): boxes of 32 rows x 64
+// columns, 128-byte swizzle.
 bool make_store_map_bf16(CUtensorMap* map, uint16_t* ptr, int64_t rows, int64_t cols) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return false;
@@ -720,7 +797,8 @@ cudaError_t max_pairs(int* pairs) {
 
 template <int EPI, bool A_MN = false, bool B_MN = false>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s,
-                   const CUtensorMap* mc = nullptr, bool pdl = false) {
+                   const CUtensorMap* mc = nullptr, bool pdl = false,
+                   const CUtensorMap* md = nullptr) {
   int pairs = 0;
   cudaError_t e = max_pairs<EPI, A_MN, B_MN>(&pairs);
   if (e != cudaSuccess) return e;
@@ -739,7 +817,8 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, A_MN, B_MN>, ma, mb, mc != nullptr ? *mc : ma, a);
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, A_MN, B_MN>, ma, mb, mc != nullptr ? *mc : ma,
+                            md != nullptr ? *md : ma, a);
 }
 
 }  // namespace
@@ -846,7 +925,12 @@ cudaError_t launch_gemm_swiglu_bwd(uint16_t* d_gu, float* stats, const uint16_t*
   if (!swiglu_args(&a, &ma, &mb, d_gu, stats, A, a_scale, W1, w_scale, M, H, K))
     return cudaErrorInvalidValue;
   a.dh = dh;
-  return launch<EPI_SWIGLU_BWD>(ma, mb, a, s);
+  // d_gu [M, 2H] written and dh [M, H] read by TMA in 32 x 64 boxes
+  CUtensorMap mc, md;
+  if (!make_store_map_bf16(&mc, d_gu, M, 2 * H) ||
+      !make_store_map_bf16(&md, const_cast<uint16_t*>(dh), M, H))
+    return cudaErrorInvalidValue;
+  return launch<EPI_SWIGLU_BWD>(ma, mb, a, s, &mc, false, &md);
 }
 
 // Self-test of the failure path: the bounded pipeline wait every GEMM role
