@@ -483,6 +483,22 @@ def bench_backward(q, torch, device, steps, warmup, peaks):
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
+
+    # the same backward accumulating into dW1 and dW2 (gradient accumulation
+    # over micro-batches): the weight-gradient epilogues read the previous dW
+    def step_acc():
+        q.qffn_ffn_backward(d_ln2, dw1, dw2, st[0:2], st[2:4], dout, d["yq"], sy, d["hq"], sh,
+                            d["w1"], d["w1_scale"], d["w2"], d["w2_scale"], N, C, H, True, ws,
+                            stream=stream)
+
+    step_acc()
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        step_acc()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_acc = a.elapsed_time(b) / steps
     # staged: the three building blocks of the chain with events between them
     dh = ws[off[0]:].view(torch.int16)
     dgu = ws[off[1]:].view(torch.int16)
@@ -509,6 +525,7 @@ def bench_backward(q, torch, device, steps, warmup, peaks):
         "ms_per_step": ms, "tflops": flop / (ms * 1e-3) / 1e12,
         "tflops_without_recompute": 12.0 * N * C * H / (ms * 1e-3) / 1e12,
         "launches_per_step": 7,
+        "ms_per_step_accumulating_dw": ms_acc,
         "stages_ms": {"backward_qmm_down": stage[0], "gate_up_swiglu_backward": stage[1],
                       "backward_qmm_up": stage[2]},
         "gate_up_swiglu_backward_tflops": 2.0 * N * C * 2 * H / (stage[1] * 1e-3) / 1e12,

@@ -80,7 +80,9 @@ constexpr int B_BYTES = KBOX * BOX_BYTES;  // this CTA's half of the B rows of a
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;
-constexpr int NUM_BARS = 2 * STAGES + 5 + 4;   // + one per epilogue warp (SwiGLU backward's dh loads)
+// + two per epilogue warp: its staging boxes' TMA loads (dh of the SwiGLU
+// backward, the previous output of the accumulating bf16 form)
+constexpr int NUM_BARS = 2 * STAGES + 5 + 8;
 // SwiGLU h staging for the TMA stores: 4 epilogue warps x 2 buffers of a
 // 32-row x 64-column bf16 box (4 KB, 128-byte swizzle)
 constexpr int STAGE_BOX_BYTES = 32 * 64 * 2;
@@ -322,8 +324,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * uint32_t(2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * uint32_t(2 * STAGES + 4);
-  //   dh[q]      epilogue warp of lane quarter q: its dh box has landed (SwiGLU backward)
-  auto dh_bar = [&](int q) { return bar0 + 8u * uint32_t(2 * STAGES + 5 + q); };
+  //   ld[q][b]   epilogue warp of lane quarter q: the TMA load into its
+  //              staging box b has landed
+  auto ld_bar = [&](int q, int b) { return bar0 + 8u * uint32_t(2 * STAGES + 5 + 2 * q + b); };
+  auto dh_bar = [&](int q) { return ld_bar(q, 0); };
 
   constexpr bool SWIGLU = EPI != EPI_BF16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -340,15 +344,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(tempty_bar(a), 8);
     }
     mbar_init(drain_bar, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(dh_bar(q), 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(ld_bar(q, 0), 1);
+      mbar_init(ld_bar(q, 1), 1);
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || (EPI == EPI_BF16 && !args.accumulate))
-      tma_prefetch_desc(&tmC);
+    if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || EPI == EPI_BF16) tma_prefetch_desc(&tmC);
     if (EPI == EPI_SWIGLU_BWD) tma_prefetch_desc(&tmD);
   }
   if (warp == 1) {
@@ -480,6 +486,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       dh_pending = true;
     };
     if (EPI == EPI_SWIGLU_BWD && lane == 0 && pair < args.num_tiles) load_dh(pair, 0);
+    // accumulating bf16 form: the previous output comes in by TMA, one 32-row
+    // x 64-column box (group g of the tile's 256 columns) into staging box
+    // g & 1, the next group's load in flight while a group is summed
+    uint32_t old_par[2] = {0u, 0u};
+    bool old_pending[2] = {false, false};   // lane 0
+    auto load_old = [&](int t, int g) {     // lane 0
+      int pmb, pnb;
+      tile_coords(t, args, pmb, pnb);
+      const int prow0 = pmb * (2 * BM) + int(rank) * BM + q * 32;
+      const int b = g & 1;
+      mbar_expect_tx(ld_bar(q, b), STAGE_BOX_BYTES);
+      tma_load_2d(smem_u32(sStaging + (q * 2 + b) * STAGE_BOX_BYTES), &tmC, ld_bar(q, b),
+                  pnb * BN + g * 64, prow0);
+      old_pending[b] = true;
+    };
+    if (EPI == EPI_BF16 && args.accumulate && lane == 0 && pair < args.num_tiles) load_old(pair, 0);
     int local = 0;
     for (int tile = pair; tile < args.num_tiles; tile += num_pairs, ++local) {
       const int acc = local & 1;
@@ -537,32 +559,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       } else if (!SWIGLU) {
-        // accumulating form (weight gradients): read-modify-write per row
-        uint16_t* orow = static_cast<uint16_t*>(args.out) + size_t(row) * size_t(args.N);
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 8) {
-          uint32_t v[8];
-          tmem_ld8(tbase + uint32_t(c0), v);
-          const int col = nb * BN + c0;
-          if (row_ok && col < args.N) {
-            uint32_t p[4];
-            if (args.bias != nullptr || args.accumulate) {
-              const uint4 b4 = args.bias != nullptr ? ld16_ro(args.bias + col) : make_uint4(0, 0, 0, 0);
-              const uint4 o4 = args.accumulate ? ld16_once(orow + col) : make_uint4(0, 0, 0, 0);
-              const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w}, ow[4] = {o4.x, o4.y, o4.z, o4.w};
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                p[j] = pack_bf16x2(
-                    (__uint_as_float(v[2 * j]) * scale + bf16_lo(bw[j])) + bf16_lo(ow[j]),
-                    (__uint_as_float(v[2 * j + 1]) * scale + bf16_hi(bw[j])) + bf16_hi(ow[j]));
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                p[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * scale, __uint_as_float(v[2 * j + 1]) * scale);
+        // accumulating form (weight gradients): out = bf16((acc + bias) + old),
+        // old from the staging box the TMA load filled, written back in place
+        // and stored by TMA
+        const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
+        bool ok = true;
+        for (int g = 0; g < BN / 64; ++g) {
+          const int b = g & 1;
+          uint8_t* box = sStaging + (q * 2 + b) * STAGE_BOX_BYTES;
+          if (g + 1 < BN / 64) {
+            if (lane == 0) {
+              bulk_wait_read_0();              // the store that last read box (g+1)&1 is done
+              load_old(tile, g + 1);
             }
-            stg16(orow + col, make_uint4(p[0], p[1], p[2], p[3]));
+            __syncwarp();
+          }
+          if (!mbar_wait(ld_bar(q, b), old_par[b], abort_flag)) { ok = false; break; }
+          old_par[b] ^= 1u;
+          if (lane == 0) old_pending[b] = false;
+#pragma unroll 1
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const int c0 = g * 64 + c8 * 8;
+            const int col = nb * BN + c0;
+            uint32_t v[8];
+            tmem_ld8(tbase + uint32_t(c0), v);
+            const uint32_t off = uint32_t(lane) * 128u + (uint32_t(c8 ^ (lane & 7)) << 4);
+            const uint4 o4 = *reinterpret_cast<const uint4*>(box + off);
+            const uint4 b4 = (args.bias != nullptr && col < args.N) ? ld16_ro(args.bias + col)
+                                                                     : make_uint4(0, 0, 0, 0);
+            const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w}, ow[4] = {o4.x, o4.y, o4.z, o4.w};
+            uint32_t p[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              p[j] = pack_bf16x2(
+                  (__uint_as_float(v[2 * j]) * scale + bf16_lo(bw[j])) + bf16_lo(ow[j]),
+                  (__uint_as_float(v[2 * j + 1]) * scale + bf16_hi(bw[j])) + bf16_hi(ow[j]));
+            *reinterpret_cast<uint4*>(box + off) = make_uint4(p[0], p[1], p[2], p[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          const int x = nb * BN + g * 64;
+          if (lane == 0) {
+            if (row0 < args.M && x < args.N) tma_store_2d(&tmC, smem_u32(box), x, row0);
+            bulk_commit();
           }
         }
+        if (!ok) break;
+        if (lane == 0) {
+          bulk_wait_read_0();                  // this tile's stores have read both boxes
+          if (tile + num_pairs < args.num_tiles) load_old(tile + num_pairs, 0);
+        }
+        __syncwarp();
       } else if (EPI == EPI_SWIGLU_BWD) {
         const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
         bool ok = true;
@@ -693,9 +740,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     // the TMA stores complete (shared memory read, global memory written) and
     // no TMA load into shared memory is in flight before exit
-    if ((EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || (EPI == EPI_BF16 && !args.accumulate)) &&
-        lane == 0)
-      bulk_wait_all();
+    if ((EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || EPI == EPI_BF16) && lane == 0) bulk_wait_all();
+    if (EPI == EPI_BF16 && args.accumulate && lane == 0)
+      for (int b = 0; b < 2; ++b)
+        if (old_pending[b]) mbar_wait(ld_bar(q, b), old_par[b], abort_flag, false, kDrainLimitNs);
     if (EPI == EPI_SWIGLU_BWD && lane == 0 && dh_pending)
       mbar_wait(dh_bar(q), dh_par, abort_flag, false, kDrainLimitNs);
     if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
@@ -848,13 +896,11 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.tiles_n = int((N + BN - 1) / BN);
   a.num_tiles = a.tiles_m * a.tiles_n;
   a.num_kb = int((K + KBOX * BK - 1) / (KBOX * BK));
-  // the output tensor map of the TMA-store epilogue (not used when accumulating)
+  // the output tensor map of the epilogue's TMA stores (and, when
+  // accumulating, of its loads of the previous output)
   CUtensorMap mc;
-  const CUtensorMap* pmc = nullptr;
-  if (!accumulate) {
-    if (!make_store_map_bf16(&mc, out, M, N)) return cudaErrorInvalidValue;
-    pmc = &mc;
-  }
+  if (!make_store_map_bf16(&mc, out, M, N)) return cudaErrorInvalidValue;
+  const CUtensorMap* pmc = &mc;
   if (a_mn && w_mn) return launch<EPI_BF16, true, true>(ma, mb, a, s, pmc, pdl);
   if (a_mn) return launch<EPI_BF16, true, false>(ma, mb, a, s, pmc, pdl);
   if (w_mn) return launch<EPI_BF16, false, true>(ma, mb, a, s, pmc, pdl);
