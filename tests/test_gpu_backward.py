@@ -65,7 +65,10 @@ def test_swiglu_backward(q, N, H):
 
 
 @pytest.mark.parametrize("N,IC,OC,acc", [(48, 96, 64, False), (64, 256, 128, True), (256, 512, 384, False),
-                                         (512, 1024, 2048, True)])
+                                         (512, 1024, 2048, True),
+                                         # accumulating with ragged tiles: IC = 160 ends inside a
+                                         # 64-column box, OC = 96 inside a 128-row half tile
+                                         (48, 160, 96, True), (272, 288, 352, True)])
 def test_backward_qmm(q, N, IC, OC, acc):
     dout = random_bf16((N, OC), seed=N + OC, std=1e-3)
     inq, ins = oracle.quantize_tensor(random_bf16((N, IC), seed=N + IC))

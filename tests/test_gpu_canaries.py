@@ -78,8 +78,9 @@ def test_gemm_and_qmm_stay_inside_their_outputs(q, M, N, K):
     out2.check("qmm out")
 
 
+@pytest.mark.parametrize("acc", [False, True])
 @pytest.mark.parametrize("N,IC,OC", [(16, 32, 32), (48, 96, 64), (272, 160, 224)])
-def test_backward_qmm_stays_inside_its_outputs(q, N, IC, OC):
+def test_backward_qmm_stays_inside_its_outputs(q, N, IC, OC, acc):
     dout = dev(random_bf16((N, OC), seed=N, std=1e-3))
     inq, ins = oracle.quantize_tensor(random_bf16((N, IC), seed=IC))
     wq, ws = oracle.quantize_tensor(random_bf16((OC, IC), seed=OC, std=0.02))
@@ -88,9 +89,11 @@ def test_backward_qmm_stays_inside_its_outputs(q, N, IC, OC):
     sc = torch.tensor([ins, ws], dtype=torch.float32, device="cuda")
     dinp = Guarded(N * IC * 2)
     dw = Guarded(OC * IC * 2)
+    if acc:   # the accumulating form reads the previous dW: give it finite values
+        dw.view(torch.int16, OC, IC).copy_(dev(random_bf16((OC, IC), seed=5, std=1e-2)))
     wsb = torch.empty(q.qffn_backward_qmm_workspace_size(N, IC, OC), dtype=torch.uint8, device="cuda")
     q.qffn_backward_qmm(dinp.view(torch.int16, N, IC), dw.view(torch.int16, OC, IC), st, dout, dev(inq), sc[0:1],
-                        dev(wq), sc[1:2], N, IC, OC, False, wsb)
+                        dev(wq), sc[1:2], N, IC, OC, acc, wsb)
     dinp.check("backward_qmm dinp")
     dw.check("backward_qmm dw")
 
