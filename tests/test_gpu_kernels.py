@@ -157,7 +157,11 @@ def _gemm_check(got, want, a, sa, w, sw, max_mismatch=1e-3):
 
 GEMM_SHAPES = [
     (1, 32, 16), (64, 256, 128), (128, 256, 128), (129, 288, 144), (300, 512, 512),
-    (256, 768, 256), (200, 256, 4096), (130, 512, 14336), (1000, 1024, 2048)]
+    (256, 768, 256), (200, 256, 4096), (130, 512, 14336), (1000, 1024, 2048),
+    # more tiles than SM pairs with a short last wave, which runs as half tiles
+    # (N = 128): 80 tiles, and 78 tiles whose split ones sit on a ragged
+    # column edge (N = 416)
+    (20480, 256, 64), (9984, 416, 96)]
 
 
 @pytest.mark.parametrize("M,N,K", GEMM_SHAPES)

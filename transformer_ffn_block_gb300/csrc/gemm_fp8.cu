@@ -103,6 +103,10 @@ constexpr uint32_t kIdesc = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t((2
 constexpr uint32_t idesc_for(bool a_mn, bool b_mn) {
   return kIdesc | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u);
 }
+// The same descriptor with another N (bits 17-22 hold N >> 3).
+constexpr uint32_t idesc_n(uint32_t idesc, int n) {
+  return (idesc & ~(0x3Fu << 17)) | (uint32_t(n >> 3) << 17);
+}
 // Byte step of one UMMA_K slice inside a stage: along the 128-byte row for a
 // K-major operand, UMMA_K rows of 128 bytes for an MN-major one.
 constexpr uint32_t kStepK = UMMA_K;
@@ -127,6 +131,11 @@ struct GemmArgs {
   int M, N, K;   // N: output columns (SwiGLU: H)
   int H;         // SwiGLU: first up row of W1
   int tiles_m, tiles_n, num_tiles, num_kb;
+  // Work units below split_from are 256-column tiles; each unit from there on
+  // is one 128-column half of the tiles split_from, split_from + 1, ...:
+  // a last partial wave of R tiles runs as 2R half tiles in half the time
+  // (bf16 form with K-major operands only; split_from = num_tiles otherwise).
+  int split_from;
 };
 
 // Bounded wait on a pipeline barrier of this kernel (status word g_status).
@@ -287,6 +296,19 @@ QFFN_DEVI void tmem_ld8x2(uint32_t ta, uint32_t tb, uint32_t (&a)[8], uint32_t (
 }
 
 // Pair tile -> (pair M-block of 256 rows, N-block)
+QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb);
+// Work unit -> (pair M-block, N-block, half): half = -1 for a whole tile,
+// 0 / 1 for the first / second 128 columns of a split one.
+QFFN_DEVI void unit_coords(int u, const GemmArgs& a, int& mb, int& nb, int& half) {
+  if (u < a.split_from) {
+    tile_coords(u, a, mb, nb);
+    half = -1;
+  } else {
+    const int h = u - a.split_from;
+    tile_coords(a.split_from + (h >> 1), a, mb, nb);
+    half = h & 1;
+  }
+}
 QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
   const int per_group = GROUP_M * a.tiles_n;
   const int group = tile / per_group;
@@ -383,15 +405,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int it = 0;
       bool ok = true;
       for (int tile = pair; ok && tile < args.num_tiles; tile += num_pairs) {
-        int mb, nb;
-        tile_coords(tile, args, mb, nb);
+        int mb, nb, half;
+        unit_coords(tile, args, mb, nb, half);
         const int rowA = mb * (2 * BM) + int(rank) * BM;
-        const int rowB = SWIGLU ? (rank == 0 ? nb * 128 : args.H + nb * 128) : nb * BN + int(rank) * 128;
+        // a half tile's B rows: 64 per CTA, from the tensor map with 64-row boxes
+        const int rowB = SWIGLU ? (rank == 0 ? nb * 128 : args.H + nb * 128)
+                         : half < 0 ? nb * BN + int(rank) * 128
+                                    : nb * BN + half * 128 + int(rank) * 64;
+        const CUtensorMap* mapB = half < 0 ? &tmB : &tmD;
+        const uint32_t stage_tx = half < 0 ? 2 * STAGE_BYTES : 2 * (A_BYTES + B_BYTES / 2);
         for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = uint32_t(it / STAGES) & 1u;
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
-          if (rank == 0) mbar_expect_tx(full_bar(s), 2 * STAGE_BYTES);
+          if (rank == 0) mbar_expect_tx(full_bar(s), stage_tx);
           const uint32_t fb = map_to_rank(full_bar(s), 0);
           // K-major: x = K offset, y = row; MN-major: x = M (N) offset, y = K row
 #pragma unroll
@@ -402,7 +429,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (A_MN) tma_load_2d_pair(da, &tmA, fb, rowA, kx);
             else tma_load_2d_pair(da, &tmA, fb, kx, rowA);
             if (B_MN) tma_load_2d_pair(db, &tmB, fb, rowB, kx);
-            else tma_load_2d_pair(db, &tmB, fb, kx, rowB);
+            else tma_load_2d_pair(db, mapB, fb, kx, rowB);
           }
           issued |= 1u << s;
           issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
@@ -427,6 +454,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        // a half tile is N = 128 (64 B rows per CTA)
+        const uint32_t idesc = tile < args.split_from ? idesc_for(A_MN, B_MN)
+                                                      : idesc_n(idesc_for(A_MN, B_MN), BN / 2);
         for (int kb = 0; kb < args.num_kb; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = uint32_t(it / STAGES) & 1u;
@@ -440,7 +470,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kk = 0; kk < BK / UMMA_K; ++kk)
               mma_f8_pair(d_tmem, sdesc_sw128(a0 + bx * BOX_BYTES + kk * (A_MN ? kStepMN : kStepK)),
                           sdesc_sw128(b0 + bx * BOX_BYTES + kk * (B_MN ? kStepMN : kStepK)),
-                          idesc_for(A_MN, B_MN), uint32_t(kb | bx | kk));
+                          idesc, uint32_t(kb | bx | kk));
           mma_commit_mc(empty_bar(s), kBothCtas);
         }
         if (!ok) break;
@@ -508,8 +538,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t aph = uint32_t(local >> 1) & 1u;
       if (!mbar_wait(tfull_bar(acc), aph, abort_flag)) break;
       tc_fence_after();
-      int mb, nb;
-      tile_coords(tile, args, mb, nb);
+      int mb, nb, half;
+      unit_coords(tile, args, mb, nb, half);
       const int row = mb * (2 * BM) + row_in_tile;
       const bool row_ok = row < args.M;
       const uint32_t tbase = tmem_base + (uint32_t(q * 32) << 16) + uint32_t(acc * BN);
@@ -521,11 +551,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // shared-memory operand reads also use.  The tensor map clips rows
         // beyond M and columns beyond N.
         const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
+        // a half tile holds 128 accumulator columns, starting at column 128 * half
+        const int cbase = nb * BN + (half < 0 ? 0 : half * (BN / 2));
+        const int ncols = half < 0 ? BN : BN / 2;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 8) {
+        for (int c0 = 0; c0 < ncols; c0 += 8) {
           uint32_t v[8];
           tmem_ld8(tbase + uint32_t(c0), v);
-          const int col = nb * BN + c0;
+          const int col = cbase + c0;
           const int chunk = (c0 & 63) >> 3;
           uint8_t* sbox = sStaging + (q * 2 + sbuf) * STAGE_BOX_BYTES;
           if (chunk == 0) {
@@ -550,7 +583,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (chunk == 7) {
             fence_proxy_async_smem();
             __syncwarp();
-            const int x = nb * BN + (c0 & ~63);
+            const int x = cbase + (c0 & ~63);
             if (lane == 0) {
               if (row0 < args.M && x < args.N) tma_store_2d(&tmC, smem_u32(sbox), x, row0);
               bulk_commit();
@@ -780,13 +813,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D E4M3 tensor [rows, k] (k contiguous), boxes of 128 rows x 128 bytes.
-bool make_map(CUtensorMap* map, const uint8_t* ptr, int64_t rows, int64_t k) {
+// 2-D E4M3 tensor [rows, k] (k contiguous), boxes of box_rows rows x 128 bytes.
+bool make_map(CUtensorMap* map, const uint8_t* ptr, int64_t rows, int64_t k,
+              uint32_t box_rows = 128) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {cuuint64_t(k), cuuint64_t(rows)};
   cuuint64_t strides[1] = {cuuint64_t(k)};
-  cuuint32_t box[2] = {cuuint32_t(BK), 128u};
+  cuuint32_t box[2] = {cuuint32_t(BK), box_rows};
   cuuint32_t estr[2] = {1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(ptr), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -896,6 +930,7 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.tiles_n = int((N + BN - 1) / BN);
   a.num_tiles = a.tiles_m * a.tiles_n;
   a.num_kb = int((K + KBOX * BK - 1) / (KBOX * BK));
+  a.split_from = a.num_tiles;
   // the output tensor map of the epilogue's TMA stores (and, when
   // accumulating, of its loads of the previous output)
   CUtensorMap mc;
@@ -904,6 +939,21 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   if (a_mn && w_mn) return launch<EPI_BF16, true, true>(ma, mb, a, s, pmc, pdl);
   if (a_mn) return launch<EPI_BF16, true, false>(ma, mb, a, s, pmc, pdl);
   if (w_mn) return launch<EPI_BF16, false, true>(ma, mb, a, s, pmc, pdl);
+  // K-major, not accumulating: a last partial wave of R <= pairs / 2 tiles
+  // runs as 2R half tiles (N = 128), so it takes half a tile's time
+  if (!accumulate) {
+    int pairs = 0;
+    cudaError_t e = max_pairs<EPI_BF16>(&pairs);
+    if (e != cudaSuccess) return e;
+    const int r = a.num_tiles % pairs;
+    if (a.num_tiles > pairs && r > 0 && 2 * r <= pairs) {
+      CUtensorMap mb_half;   // B boxes of 64 rows: a half tile's share per CTA
+      if (!make_map(&mb_half, W, N, K, 64)) return cudaErrorInvalidValue;
+      a.split_from = a.num_tiles - r;
+      a.num_tiles += r;
+      return launch<EPI_BF16>(ma, mb, a, s, pmc, pdl, &mb_half);
+    }
+  }
   return launch<EPI_BF16>(ma, mb, a, s, pmc, pdl);
 }
 
@@ -926,6 +976,7 @@ bool swiglu_args(GemmArgs* a, CUtensorMap* ma, CUtensorMap* mb, void* out, float
   a->tiles_n = int(H / 128);
   a->num_tiles = a->tiles_m * a->tiles_n;
   a->num_kb = int((K + KBOX * BK - 1) / (KBOX * BK));
+  a->split_from = a->num_tiles;
   return true;
 }
 }  // namespace
