@@ -209,7 +209,11 @@ qffn_status qffn_gate_up_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t
  * 256-byte aligned, holding y, yq, h, hq at the offsets that
  * qffn_forward_workspace_offsets() returns (readable after the call).
  * N = B*T >= 0, C % 128 == 0, H % 128 == 0, 128 <= C <= 16384,
- * 128 <= H <= 2^20. */
+ * 128 <= H <= 2^20.
+ * Five kernels (and one 4-byte memset) on `stream`; the four after the norm
+ * are programmatic dependent launches, scheduled while their predecessor
+ * drains and waiting for it before touching memory (no effect on results;
+ * stream capture keeps the edges). */
 size_t qffn_forward_workspace_size(int64_t B, int64_t T, int64_t C, int64_t H);
 qffn_status qffn_forward_workspace_offsets(int64_t B, int64_t T, int64_t C, int64_t H,
                                            size_t offsets[4] /* y, yq, h, hq */);
