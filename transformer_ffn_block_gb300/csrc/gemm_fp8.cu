@@ -498,6 +498,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       qinv = qzero ? 0.0f : 448.0f / given;
       if (blockIdx.x == 0 && threadIdx.x == 64) args.amax[1] = qzero ? 1.0f : given / 448.0f;
     }
+    // (The two forms below that prefetch by TMA run whole tiles only -- the
+    // host splits a short last wave only for the plain bf16 form -- so their
+    // work units map to tiles one to one.)
     // EPI_SWIGLU_BWD: dh comes in by TMA, one 32-row x 64-column box per warp
     // and half tile, into staging box A of the warp; dg is written back over
     // it and du into box B, and both go out by TMA stores.  The first half's
