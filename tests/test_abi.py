@@ -192,3 +192,79 @@ def test_bounded_wait_selftest_argument_checks(lib):
     assert f(A, 0, 99999, None) == 1                  # below 100 us
     assert f(A, 0, 2000000001, None) == 1             # above 2 s
     assert f(A + 4, 0, 1000000, None) == 3            # out not 8-byte aligned
+
+
+# Every call below fails one host-side check, so nothing is ever enqueued with
+# the fake addresses.
+
+def test_absmax_argument_checks(lib):
+    f = lambda *a: _call(lib, "qffn_absmax", *a)
+    assert f(NULL, A, 16, None) == 1
+    assert f(A, NULL, 16, None) == 1
+    assert f(A, A, -1, None) == 1
+    assert f(A + 2, A, 16, None) == 3                   # stats: 4-byte alignment
+    assert f(A, MIS, 16, None) == 3                     # input: 16-byte alignment
+
+
+def test_gemv_dual_argument_checks(lib):
+    f = lambda *a: _call(lib, "qffn_gemv_dual", *a)
+    good = [A, A, A, A, A, A, A, 64, 256, None]         # g, u, x, w_gate, s_gate, w_up, s_up, H, C
+    for i in range(7):
+        bad = list(good)
+        bad[i] = NULL
+        assert f(*bad) == 1, i
+    assert f(A, A, A, A, A, A, A, 0, 256, None) == 1    # H >= 1
+    assert f(A, A, A, A, A, A, A, 64, 24, None) == 2    # C % 16
+    assert f(A, A, A, A, A, A, A, 64, 32784, None) == 2  # C > 32768
+    assert f(A, A, MIS, A, A, A, A, 64, 256, None) == 3  # x
+    assert f(A, A, A, MIS, A, A, A, 64, 256, None) == 3  # w_gate
+    assert f(A, A, A, A, A + 2, A, A, 64, 256, None) == 3  # s_gate
+
+
+def test_decode_noalloc_argument_checks(lib):
+    f = lambda *a: _call(lib, "qffn_decode_forward_noalloc", *a)
+    good = [A, A, A, A, A, A, A, A, 256, 768, None]     # out, x, wg, sg, wu, su, wd, sd, C, H
+    for i in range(8):
+        bad = list(good)
+        bad[i] = NULL
+        assert f(*bad) == 1, i
+    assert f(A, A, A, A, A, A, A, A, 24, 768, None) == 2      # C % 16
+    assert f(A, A, A, A, A, A, A, A, 256, 32784, None) == 2   # H above the library's scratch
+    assert f(A, MIS, A, A, A, A, A, A, 256, 768, None) == 3   # x
+    assert f(A, A, A, A + 2, A, A, A, A, 256, 768, None) == 3  # s_gate
+
+
+def test_gate_up_swiglu_backward_argument_checks(lib):
+    f = lambda *a: _call(lib, "qffn_gate_up_swiglu_backward", *a)
+    # d_gate_up, stats, dh, yq, y_scale, w1, w1_scale, N, C, H
+    assert f(NULL, A, A, A, A, A, A, 64, 256, 768, None) == 1
+    assert f(A, A, NULL, A, A, A, A, 64, 256, 768, None) == 1
+    assert f(A, A, A, A, A, A, A, -1, 256, 768, None) == 1
+    assert f(A, A, A, A, A, A, A, 64, 24, 768, None) == 2       # C % 16
+    assert f(A, A, A, A, A, A, A, 64, 256, 200, None) == 2      # H % 128
+    assert f(A, A + 2, A, A, A, A, A, 64, 256, 768, None) == 3  # stats
+    assert f(A, A, MIS, A, A, A, A, 64, 256, 768, None) == 3    # dh
+
+
+def test_ffn_backward_argument_checks(lib):
+    f = lambda *a: _call(lib, "qffn_ffn_backward", *a)
+    ws = lib.qffn_ffn_backward_workspace_size(64, 256, 768)
+    # 14 pointers, N, C, H, accumulate, workspace, workspace_bytes
+    good = [A] * 14 + [64, 256, 768, 0, A, ws, None]
+
+    def call(**kw):
+        args = list(good)
+        for i, v in kw.items():
+            args[int(i[1:])] = v
+        return f(*args)
+
+    assert call(p0=NULL) == 1                           # d_ln2
+    assert call(p13=NULL) == 1                          # w2_scale
+    assert call(p18=NULL) == 1                          # workspace
+    assert call(p14=-1) == 1                            # N
+    assert call(p16=200) == 2                           # H % 128
+    assert call(p14=60) == 2                            # N % 16
+    assert call(p19=ws - 1) == 1                        # workspace too small
+    assert call(p18=A + 16) == 3                        # workspace 256-byte alignment
+    assert call(p0=MIS) == 3                            # d_ln2
+    assert call(p3=A + 2) == 3                          # stats_dout
