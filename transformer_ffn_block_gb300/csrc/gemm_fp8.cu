@@ -134,7 +134,8 @@ struct GemmArgs {
   // Work units below split_from are 256-column tiles; each unit from there on
   // is one 128-column half of the tiles split_from, split_from + 1, ...:
   // a last partial wave of R tiles runs as 2R half tiles in half the time
-  // (bf16 form with K-major operands only; split_from = num_tiles otherwise).
+  // (the bf16 form with K-major operands that does not accumulate, and the
+  // SwiGLU forward forms; split_from = num_tiles otherwise).
   int split_from;
 };
 
@@ -409,7 +410,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         unit_coords(tile, args, mb, nb, half);
         const int rowA = mb * (2 * BM) + int(rank) * BM;
         // a half tile's B rows: 64 per CTA, from the tensor map with 64-row boxes
-        const int rowB = SWIGLU ? (rank == 0 ? nb * 128 : args.H + nb * 128)
+        // SwiGLU: CTA 0 stages gate rows, CTA 1 the matching up rows (64 of
+        // each in a half tile)
+        const int rowB = SWIGLU ? (half < 0 ? (rank == 0 ? nb * 128 : args.H + nb * 128)
+                                            : (rank == 0 ? 0 : args.H) + nb * 128 + half * 64)
                          : half < 0 ? nb * BN + int(rank) * 128
                                     : nb * BN + half * 128 + int(rank) * 64;
         const CUtensorMap* mapB = half < 0 ? &tmB : &tmD;
@@ -499,8 +503,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (blockIdx.x == 0 && threadIdx.x == 64) args.amax[1] = qzero ? 1.0f : given / 448.0f;
     }
     // (The two forms below that prefetch by TMA run whole tiles only -- the
-    // host splits a short last wave only for the plain bf16 form -- so their
-    // work units map to tiles one to one.)
+    // host does not split their last wave -- so their work units map to
+    // tiles one to one.)
     // EPI_SWIGLU_BWD: dh comes in by TMA, one 32-row x 64-column box per warp
     // and half tile, into staging box A of the warp; dg is written back over
     // it and du into box B, and both go out by TMA stores.  The first half's
@@ -706,7 +710,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
       } else {
-        const size_t hoff = size_t(row) * size_t(args.N) + size_t(nb) * 128;
+        // a half tile holds 64 gate columns then the 64 matching up columns
+        const int hbase = half < 0 ? 0 : half * 64;          // first h column of the unit
+        const int hcols = half < 0 ? 128 : 64;
+        const int up_off = half < 0 ? 128 : 64;               // accumulator column of u
+        const size_t hoff = size_t(row) * size_t(args.N) + size_t(nb) * 128 + size_t(hbase);
         uint8_t* qrow = static_cast<uint8_t*>(args.out) + hoff;
         // Eight columns of g and u per step in a rolled loop: the epilogue's
         // code stays small, so it does not crowd the producer's and the MMA
@@ -714,9 +722,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // it shares with them (measured: 2.4% fewer cycles per GEMM than a
         // fully unrolled 32-column step).
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 8) {
+        for (int c0 = 0; c0 < hcols; c0 += 8) {
           uint32_t g[8], u[8];
-          tmem_ld8x2(tbase + uint32_t(c0), tbase + uint32_t(128 + c0), g, u);
+          tmem_ld8x2(tbase + uint32_t(c0), tbase + uint32_t(up_off + c0), g, u);
           {
             // EPI_SWIGLU stages h in shared memory and stores it with TMA, one
             // 32-row x 64-column box per warp and half tile: each lane writes
@@ -748,7 +756,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
                 if (lane == 0) {
-                  if (row0 < args.M) tma_store_2d(&tmC, smem_u32(sbox), nb * 128 + (c0 & ~63), row0);
+                  if (row0 < args.M)
+                    tma_store_2d(&tmC, smem_u32(sbox), nb * 128 + hbase + (c0 & ~63), row0);
                   bulk_commit();
                 }
                 sbuf ^= 1;
@@ -906,6 +915,25 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
                             md != nullptr ? *md : ma, a);
 }
 
+// A last partial wave of R <= pairs / 2 tiles runs as 2R half tiles (N = 128)
+// in half a tile's time: sets split_from and num_tiles, and the weight tensor
+// map with 64-row boxes that the half tiles' B loads use.  Leaves the
+// arguments unchanged otherwise.
+template <int EPI>
+cudaError_t split_last_wave(GemmArgs* a, CUtensorMap* mb_half, const uint8_t* W, int64_t wrows,
+                            int64_t K) {
+  int pairs = 0;
+  cudaError_t e = max_pairs<EPI>(&pairs);
+  if (e != cudaSuccess) return e;
+  const int r = a->num_tiles % pairs;
+  if (a->num_tiles > pairs && r > 0 && 2 * r <= pairs) {
+    if (!make_map(mb_half, W, wrows, K, 64)) return cudaErrorInvalidValue;
+    a->split_from = a->num_tiles - r;
+    a->num_tiles += r;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_scale,
@@ -942,22 +970,13 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   if (a_mn && w_mn) return launch<EPI_BF16, true, true>(ma, mb, a, s, pmc, pdl);
   if (a_mn) return launch<EPI_BF16, true, false>(ma, mb, a, s, pmc, pdl);
   if (w_mn) return launch<EPI_BF16, false, true>(ma, mb, a, s, pmc, pdl);
-  // K-major, not accumulating: a last partial wave of R <= pairs / 2 tiles
-  // runs as 2R half tiles (N = 128), so it takes half a tile's time
+  // K-major, not accumulating: a short last wave runs as half tiles
+  CUtensorMap mb_half;
   if (!accumulate) {
-    int pairs = 0;
-    cudaError_t e = max_pairs<EPI_BF16>(&pairs);
+    cudaError_t e = split_last_wave<EPI_BF16>(&a, &mb_half, W, N, K);
     if (e != cudaSuccess) return e;
-    const int r = a.num_tiles % pairs;
-    if (a.num_tiles > pairs && r > 0 && 2 * r <= pairs) {
-      CUtensorMap mb_half;   // B boxes of 64 rows: a half tile's share per CTA
-      if (!make_map(&mb_half, W, N, K, 64)) return cudaErrorInvalidValue;
-      a.split_from = a.num_tiles - r;
-      a.num_tiles += r;
-      return launch<EPI_BF16>(ma, mb, a, s, pmc, pdl, &mb_half);
-    }
   }
-  return launch<EPI_BF16>(ma, mb, a, s, pmc, pdl);
+  return launch<EPI_BF16>(ma, mb, a, s, pmc, pdl, a.split_from < a.num_tiles ? &mb_half : nullptr);
 }
 
 namespace {
@@ -998,7 +1017,11 @@ cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, co
     return cudaErrorInvalidValue;
   CUtensorMap mc;
   if (!make_store_map_bf16(&mc, h, M, H)) return cudaErrorInvalidValue;
-  return launch<EPI_SWIGLU>(ma, mb, a, s, &mc, chained);
+  CUtensorMap mb_half;
+  cudaError_t e = split_last_wave<EPI_SWIGLU>(&a, &mb_half, W1, 2 * H, K);
+  if (e != cudaSuccess) return e;
+  return launch<EPI_SWIGLU>(ma, mb, a, s, &mc, chained,
+                            a.split_from < a.num_tiles ? &mb_half : nullptr);
 }
 
 cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t* A,
@@ -1011,7 +1034,11 @@ cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t*
   GemmArgs a;
   if (!swiglu_args(&a, &ma, &mb, hq, stats_h, A, a_scale, W1, w_scale, M, H, K))
     return cudaErrorInvalidValue;
-  return launch<EPI_SWIGLU_E4M3>(ma, mb, a, s, nullptr, pdl);
+  CUtensorMap mb_half;
+  cudaError_t e = split_last_wave<EPI_SWIGLU_E4M3>(&a, &mb_half, W1, 2 * H, K);
+  if (e != cudaSuccess) return e;
+  return launch<EPI_SWIGLU_E4M3>(ma, mb, a, s, nullptr, pdl,
+                                 a.split_from < a.num_tiles ? &mb_half : nullptr);
 }
 
 cudaError_t launch_gemm_swiglu_bwd(uint16_t* d_gu, float* stats, const uint16_t* dh,
