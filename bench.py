@@ -40,8 +40,8 @@ L2_BYTES = 129 * 1024 * 1024
 FP8_PER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor rate ratio
 # DRAM bytes (read + write) per launch of the dominant kernels, from one ncu
 # capture of this benchmark's full-size workload (dram__bytes_read.sum +
-# dram__bytes_write.sum, summarised in profiles/launches_llama3-8b_ffn.md).
-# Set to None whenever the kernel changes until it is captured again.
+# dram__bytes_write.sum).  Set to None whenever the kernel changes until it
+# is captured again.
 TRAFFIC_GATE_UP_BYTES = (1006.4 + 445.8) * 1e6
 TRAFFIC_DUAL_GEMV_BYTES = (117.6 + 0.1) * 1e6
 
@@ -155,8 +155,8 @@ def to_dev(a, torch, device):
     return t.to(device)
 
 
-def prefill_setup(q, torch, device):
-    cfg = PREFILL_CFG
+def prefill_setup(q, torch, device, cfg=None):
+    cfg = cfg or PREFILL_CFG
     inp = prefill_inputs(cfg)
     N, C, H = cfg.N, cfg.C, cfg.H
     d = {}
@@ -188,16 +188,16 @@ def prefill_setup(q, torch, device):
     return d
 
 
-def forward(q, d, stream):
-    cfg = PREFILL_CFG
+def forward(q, d, stream, cfg=None):
+    cfg = cfg or PREFILL_CFG
     q.qffn_forward(d["res_out"], d["out"], d["rstd"], d["stats"][0:2], d["stats"][2:4], d["res"],
                    d["x"], d["gain"], cfg.eps, d["w1"], d["w1_scale"], d["w2"], d["w2_scale"],
                    cfg.B, cfg.T, cfg.C, cfg.H, d["ws"], stream=stream)
 
 
-def staged_forward(q, d, stream, ev):
+def staged_forward(q, d, stream, ev, cfg=None):
     """The launches of qffn_forward, issued stage by stage with events between them."""
-    cfg = PREFILL_CFG
+    cfg = cfg or PREFILL_CFG
     N, C, H = cfg.N, cfg.C, cfg.H
     st = d["stats"]
     ev[0].record(stream)
@@ -377,6 +377,48 @@ def bench_prefill(q, torch, device, steps, warmup, dist, peaks):
         "gate_up_swiglu_e4m3_gemm_ms": ms_gq,
         "gate_up_swiglu_e4m3_gemm_tflops": gate_up_flop / (ms_gq * 1e-3) / 1e12,
     }
+    return res
+
+
+def bench_workload(q, torch, device, cfg, steps, warmup, peaks):
+    """The prefill chain on another of the pages' workload shapes: whole-chain time through
+    qffn_forward and the gate|up GEMM's own time from a staged pass."""
+    d = prefill_setup(q, torch, device, cfg)
+    stream = torch.cuda.Stream(device)
+    N, C, H = cfg.N, cfg.C, cfg.H
+    for _ in range(warmup):
+        forward(q, d, stream, cfg)
+    torch.cuda.synchronize()
+    q.qffn_check_status(stream)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    # small workloads run in microseconds: more steps for a stable figure
+    reps = steps if cfg.gemm_flop >= 1e11 else max(steps, 500)
+    t0.record(stream)
+    for _ in range(reps):
+        forward(q, d, stream, cfg)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / reps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for i in range(steps):
+        staged_forward(q, d, stream, evs[i], cfg)
+    torch.cuda.synchronize()
+    q.qffn_check_status(stream)
+    stage_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(5)]
+    gate_up = 2 * N * C * 2 * H / (stage_ms[2] * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    ws_bytes = 8 * N * C + 2 * C + 3 * H * C + 4 * N            # inputs, weights and outputs once
+    res = {"workload": f"{cfg.name}: B={cfg.B}, T={cfg.T} (N={N}), C={C}, H={H}",
+           "ms_per_step": ms, "tflops": cfg.gemm_flop / (ms * 1e-3) / 1e12, "steps": reps,
+           "gate_up_ms": stage_ms[2], "gate_up_tflops": gate_up,
+           "gate_up_roofline_frac": gate_up / peak,
+           "stages_ms": dict(zip(["rmsnorm_absmax", "quantize_y", "gate_up_swiglu", "quantize_h",
+                                  "down_gemm"], stage_ms)),
+           "l2": "working set larger than L2" if ws_bytes > L2_BYTES
+           else "working set fits in L2 (resident across steps)"}
+    del d
+    torch.cuda.empty_cache()
     return res
 
 
@@ -663,47 +705,53 @@ def bench_decode(q, torch, device, iters, dist, peaks):
 
 
 # ---------------------------------------------------------------- CPU oracle legs
-def oracle_prefill_sample(tokens: int):
-    """Run the oracle chain on the first `tokens` tokens of the 8B workload; returns seconds."""
-    import oracle
-    cfg = PREFILL_CFG
-    inp = prefill_inputs(cfg)
-    w1q, w1s = oracle.quantize_tensor(inp["w1"])
-    w2q, w2s = oracle.quantize_tensor(inp["w2"])
-    t = time.perf_counter()
-    oracle.ffn_forward(inp["res"][:tokens], inp["x"][:tokens], inp["gain"], inp["eps"], w1q, w1s,
-                       w2q, w2s, cfg.H)
-    return time.perf_counter() - t
+def _oracle_bytes(cfg, tokens):
+    """Algorithmic bytes of the chain on `tokens` tokens: res, x in; r, out out (bf16);
+    rstd; gain and both FP8 weight matrices read once."""
+    C, H = cfg.C, cfg.H
+    return 8 * tokens * C + 4 * tokens + 2 * C + 3 * H * C
 
 
-def oracle_threads():
-    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
-        if os.environ.get(k):
-            return int(os.environ[k])
-    return os.cpu_count() or 1
-
-
-def cpu_baseline(budget_s: float = 12.0):
-    cfg = PREFILL_CFG
-    per_tok = cfg.gemm_flop / cfg.N
-    tokens, secs = 64, 0.0
-    import oracle  # noqa: F401
-    inp = prefill_inputs(cfg)
+def oracle_time(cfg, tokens, threads):
+    """The C++ oracle's prefill chain on the first `tokens` tokens of `cfg` with `threads`
+    OpenMP threads (0 = every processor); the library's own steady-clock time."""
     import oracle as o
+    inp = prefill_inputs(cfg)
     w1q, w1s = o.quantize_tensor(inp["w1"])
     w2q, w2s = o.quantize_tensor(inp["w2"])
-    while True:
-        t = time.perf_counter()
+    n0 = o.max_threads()
+    o.set_threads(threads)
+    used = o.max_threads()
+    try:
+        t = {}
         o.ffn_forward(inp["res"][:tokens], inp["x"][:tokens], inp["gain"], inp["eps"], w1q, w1s, w2q,
-                      w2s, cfg.H)
-        secs = time.perf_counter() - t
-        if secs * 2.2 > budget_s or tokens * 2 > cfg.N:
-            break
-        tokens *= 2
-    return {"value": per_tok * tokens / secs / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(),
-            "kind": "oracle",
-            "sample": f"oracle chain (numpy float64) on the first {tokens} of {cfg.N} tokens of the "
-                      f"Llama-3-8B FFN workload, weights pre-quantised; {secs:.2f} s"}
+                      w2s, cfg.H, timing=t)
+    finally:
+        o.set_threads(n0)
+    secs = t["seconds"]
+    flop = cfg.gemm_flop / cfg.N * tokens
+    return {"workload": cfg.name, "tokens": tokens, "of_tokens": cfg.N, "threads": used,
+            "seconds": secs, "gflops": flop / secs / 1e9,
+            "gbs": _oracle_bytes(cfg, tokens) / secs / 1e9}
+
+
+def cpu_baseline():
+    """The oracle on the host cores: every workload, bounded samples (about 20-30 s in all).
+    tiny in full and the Llama-3.2-1B sample single-threaded and on every core; the 8B
+    sample (the headline figure) on every core."""
+    runs = [oracle_time(PREFILL["tiny"], PREFILL["tiny"].N, 1),
+            oracle_time(PREFILL["tiny"], PREFILL["tiny"].N, 0),
+            oracle_time(PREFILL["llama3.2-1b"], 16, 1),
+            oracle_time(PREFILL["llama3.2-1b"], 256, 0),
+            oracle_time(PREFILL["qwen2.5-7b"], 64, 0)]
+    head = oracle_time(PREFILL_CFG, 128, 0)
+    runs.append(head)
+    return {"value": head["gflops"] / 1e3, "unit": "TFLOP/s", "cores": head["threads"], "kind": "oracle",
+            "sample": f"C++ oracle chain (exact int64 GEMM sums, fp64 norm/SwiGLU) on the first "
+                      f"{head['tokens']} of {PREFILL_CFG.N} tokens of the Llama-3-8B FFN workload, weights "
+                      f"pre-quantised, {head['threads']} OpenMP threads (os.cpu_count() = {os.cpu_count()}); "
+                      f"{head['seconds']:.2f} s by std::chrono::steady_clock",
+            "runs": runs}
 
 
 def run_reference(args, rank, world, dist):
@@ -714,29 +762,31 @@ def run_reference(args, rank, world, dist):
     inp = prefill_inputs(cfg)
     w1q, w1s = o.quantize_tensor(inp["w1"])
     w2q, w2s = o.quantize_tensor(inp["w2"])
-    tokens = 128
+    o.set_threads(0)
+    tokens = 64
     per_tok = cfg.gemm_flop / cfg.N
 
     def step():
+        t = {}
         o.ffn_forward(inp["res"][:tokens], inp["x"][:tokens], inp["gain"], inp["eps"], w1q, w1s,
-                      w2q, w2s, cfg.H)
+                      w2q, w2s, cfg.H, timing=t)
+        return t["seconds"]
 
     for _ in range(args.warmup):
         step()
-    t = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    secs = time.perf_counter() - t
+    secs = sum(step() for _ in range(args.steps))
     value = per_tok * tokens * args.steps / secs / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int64 exact GEMM sums, f64 elementwise",
         "data": "synthetic",
         "config": {"workload": f"llama3-8b FFN fwd, {tokens}-token sample per step (of N={cfg.N}), "
                                f"C={cfg.C}, H={cfg.H}", "global_batch": tokens, "seq_len": cfg.T},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
-                         "sample": f"first {tokens} tokens of the 8B workload per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": o.max_threads(), "kind": "oracle",
+                         "sample": f"C++ oracle, first {tokens} tokens of the 8B workload per step, "
+                                   f"{o.max_threads()} OpenMP threads, std::chrono::steady_clock"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -833,6 +883,8 @@ def main():
     att = bench_attention_projections(q, torch, device, args.steps, args.warmup)
     bwd = bench_backward(q, torch, device, max(3, args.steps // 4), args.warmup, peaks)
     ceiling = fp8_library_ceiling(torch, device)
+    workloads = {name: bench_workload(q, torch, device, PREFILL[name], max(5, args.steps // 2), args.warmup, peaks)
+                 for name in ("tiny", "llama3.2-1b", "qwen2.5-7b")}
     cfg = PREFILL_CFG
     value = job_throughput(cfg.gemm_flop, world, pre["ms_per_step"])
     e2e_value = job_throughput(cfg.gemm_flop, world, pre["e2e_ms"])
@@ -857,6 +909,7 @@ def main():
         "backward": bwd,
         "fp8_library_ceiling": ceiling,
         "decode": dec,
+        "workloads": workloads,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()

@@ -5,7 +5,8 @@ import torch
 
 import oracle
 from ffn_inputs import DECODE, DecodeConfig, decode_inputs
-from gpu_util import assert_out_close, bf, bf16_ulp_diff, check_dot_outputs, dev, empty_bf16, host, sync
+from gpu_util import (ACC_REL_FMA, assert_out_close, bf, bf16_ulp_diff, check_dot_outputs, dev, empty_bf16,
+                      host, sync)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +56,8 @@ def test_decode_forward(q, C, H):
     xa = np.abs(oracle.bf16_to_f64(di["x"]))
     for got, want, (wq, ws_) in ((gb, ref["g"], ref_rec["w_gate"]), (ub, ref["u"], ref_rec["w_up"])):
         absdot = (np.abs(oracle.e4m3_decode(wq)) @ xa) * ws_.astype(np.float64)
-        check_dot_outputs(got, want, absdot, cfg.C, max_mismatch=0.02)
+        check_dot_outputs(got, oracle.gemv_exact(di["x"], wq, ws_), absdot, cfg.C, 1e-3, acc_rel=ACC_REL_FMA,
+                          want_bits=want)
     vec = (2 * cfg.H + 255) // 256 * 256
     h_ws = bf(ws[:2 * cfg.H].view(torch.int16))
     np.testing.assert_array_equal(bf(ws[vec:vec + 2 * cfg.H].view(torch.int16)), ub)
@@ -63,7 +65,8 @@ def test_decode_forward(q, C, H):
     out_stage = oracle.gemv_row_scaled(h_ws, *ref_rec["w_down"])
     absdot = (np.abs(oracle.e4m3_decode(ref_rec["w_down"][0])) @ np.abs(oracle.bf16_to_f64(h_ws))) \
         * ref_rec["w_down"][1].astype(np.float64)
-    check_dot_outputs(bf(out), out_stage, absdot, cfg.H, max_mismatch=0.02)
+    check_dot_outputs(bf(out), oracle.gemv_exact(h_ws, *ref_rec["w_down"]), absdot, cfg.H, 1e-3,
+                      acc_rel=ACC_REL_FMA, want_bits=out_stage)
     # h in the workspace is exactly what the silu_mul entry point makes of g, u
     g2 = g.clone()
     q.qffn_silu_mul(g2, u, cfg.H)

@@ -1,9 +1,10 @@
 """End-to-end GPU parity of qffn_forward (the whole prefill chain A1..A5).
 
-Small and medium workloads are compared with the oracle over every element;
-the Qwen2.5-7B-shaped and Llama-3-8B workloads run at full size and are
-checked on sampled rows stage by stage (each stage fed the GPU's own
-upstream tensor) plus whole-tensor properties computed on the device.
+The tiny, Llama-3.2-1B and ragged workloads are compared with the oracle over
+every element.  The Qwen2.5-7B-shaped and Llama-3-8B workloads run at full
+size: the norm, the quantised y and both per-tensor abs-maxes are compared
+with the oracle's own over the whole tensor, and sampled rows stage by stage
+(each stage fed the GPU's own upstream tensor) and end to end.
 """
 import numpy as np
 import pytest
@@ -11,8 +12,8 @@ import torch
 
 import oracle
 from ffn_inputs import PREFILL, PrefillConfig, prefill_inputs
-from gpu_util import (assert_out_close, bf, bf16_ulp_diff, check_dot_outputs, dev, e4m3_step_diff,
-                      empty_bf16, host, sync)
+from gpu_util import (absdot_gemm, assert_out_close, bf, bf16_ulp_diff, check_codes_rule, check_dot_outputs,
+                      dev, empty_bf16, gemm_mismatch_bar, host, sync)
 
 pytestmark = pytest.mark.gpu
 
@@ -57,13 +58,16 @@ def run_forward(q, cfg, inp, with_res=True):
                 w1=w1, s1=s1, w2=w2, s2=s2)
 
 
-def check_gemm_stage(got, a, sa, w, sw, max_mismatch=2e-3):
-    want = oracle.fp8_gemm_scaled(a, sa, w, sw)
-    absdot = (np.abs(oracle.e4m3_decode(a)) @ np.abs(oracle.e4m3_decode(w)).T) * float(sa) * float(sw)
-    check_dot_outputs(got, want, absdot, a.shape[1], max_mismatch)
+def check_gemm_stage(got, a, sa, w, sw):
+    """A GEMM stage fed the GPU's own operand codes: every output within the
+    accumulation bound of the exact value, and at most the K-dependent fraction
+    of outputs differing from the exactly rounded one."""
+    K = a.shape[1]
+    check_dot_outputs(got, oracle.fp8_gemm_exact(a, sa, w, sw), absdot_gemm(a, sa, w, sw), K,
+                      gemm_mismatch_bar(K))
 
 
-def check_h_stage(q, g, yq_rows, h_rows, st, w1q, w1s, H, rows=None):
+def check_h_stage(q, g, yq_rows, h_rows, st, w1q, w1s, H):
     """h rows against SwiGLU of the GPU's unfused gate|up GEMM on the same yq rows."""
     M, C = yq_rows.shape
     gu = empty_bf16(M, 2 * H)
@@ -90,10 +94,10 @@ def check_full(q, cfg, with_res=True):
     st = host(g["stats"])
     y, yq, h, hq = bf(g["y"]), host(g["yq"]), bf(g["h"]), host(g["hq"])
 
-    # A1
+    # A1, A2: bit-exact
     if with_res:
         np.testing.assert_array_equal(bf(g["res_out"]), ref["r"])
-    np.testing.assert_array_equal(y, ref["y"])                                  # bit-exact
+    np.testing.assert_array_equal(y, ref["y"])
     np.testing.assert_allclose(host(g["rstd"]), ref["rstd"], rtol=2.0 ** -23, atol=0)
     np.testing.assert_array_equal(st[0:2], ref["stats_y"])                     # abs-max, scale
     np.testing.assert_array_equal(yq, ref["yq"])                               # codes
@@ -105,8 +109,9 @@ def check_full(q, cfg, with_res=True):
     codes, scale = oracle.quantize_with_abs_max(h, st[2])
     np.testing.assert_array_equal(hq, codes)
     assert st[3] == scale
-    dq = e4m3_step_diff(hq, ref["hq"])
-    assert (dq > 0).mean() <= 2e-3
+    # end to end against the oracle: abs-max and scale of h bit-exact, the FP8 code rule
+    np.testing.assert_array_equal(st[2:4], ref["stats_h"])
+    check_codes_rule(hq, ref["hq"])
     # A5 from the GPU's own hq
     out = bf(g["out"])
     check_gemm_stage(out, hq, st[3], w2q, w2s)
@@ -114,14 +119,106 @@ def check_full(q, cfg, with_res=True):
     return assert_out_close(out, ref["out"])
 
 
+def oracle_whole_amax_h(q, g, yq, sy, w1q, w1s, H, chunk=1024):
+    """The oracle's own abs-max of h over the whole tensor, found without the oracle
+    computing every row.
+
+    The GPU's unfused gate|up GEMM gives g', u' for every element.  The exact
+    values lie within the accumulation bound of those (the rule the GEMM stage
+    checks), with sum|terms| bounded by Cauchy-Schwarz: sa sw |yq row| |w1 row|.
+    From that, each element gets an upper bound UB on the oracle's |h| (using
+    |silu(z)| <= max(|z|, 0.28)).  The oracle computes in full the row holding
+    the GPU's largest |h| (a lower bound A0 on its own abs-max) and then every
+    row with an element whose UB reaches A0; no other row can hold its maximum.
+    Returns (oracle abs-max, number of rows the oracle computed)."""
+    N, C = yq.shape
+    ya = np.sqrt(np.sum(oracle.e4m3_decode(yq) ** 2, axis=1))                # [N]
+    wa = np.sqrt(np.sum(oracle.e4m3_decode(w1q) ** 2, axis=1))               # [2H]
+    k = (C * 2.0 ** -23 + 2.0 ** -22) * float(sy) * float(w1s)
+    lift = 1.0 + 2.0 ** -8                                                   # one bf16 rounding up
+    ub_row = np.zeros(N)
+    for r0 in range(0, N, chunk):
+        r1 = min(N, r0 + chunk)
+        gu = empty_bf16(r1 - r0, 2 * H)
+        q.qffn_fp8_gemm_scaled(gu, dev(yq[r0:r1]), g["stats"][1:2], g["w1"], g["s1"][1:2], r1 - r0, 2 * H, C)
+        sync()
+        v = oracle.bf16_to_f64(bf(gu))
+        del gu
+        bnd = k * ya[r0:r1, None] * wa[None, :]
+        bnd += 0.5 * np.ldexp(1.0, np.frexp(np.maximum(np.abs(v), 2.0 ** -126))[1] - 8) + 2.0 ** -24 * np.abs(v)
+        mag = (np.abs(v) + bnd) * lift
+        ub = np.maximum(mag[:, :H], 0.2785) * mag[:, H:] * lift * lift
+        ub_row[r0:r1] = ub.max(axis=1)
+        del v, bnd, mag, ub
+    gpu_arg = int(torch.argmax(g["h"].view(torch.bfloat16).float().abs().amax(dim=1)).item())
+
+    def oracle_rows_max(rows):
+        gu_o = oracle.fp8_gemm_scaled(yq[rows], sy, w1q, w1s)
+        return float(oracle.swiglu(gu_o, H)[1])
+
+    a0 = oracle_rows_max(np.array([gpu_arg]))
+    cand = np.nonzero(ub_row >= a0)[0]
+    return max(a0, oracle_rows_max(cand)), len(cand)
+
+
+def check_sampled(q, cfg, rows):
+    """Full-size workload in the benchmark's launch configuration: whole-tensor checks
+    of A1, A2 and of both abs-maxes against the oracle's own, then sampled rows stage
+    by stage and end to end."""
+    inp = prefill_inputs(cfg)
+    g = run_forward(q, cfg, inp)
+    N, H = cfg.N, cfg.H
+    st = host(g["stats"])
+    w1q, w1s = oracle.quantize_tensor(inp["w1"])
+    w2q, w2s = oracle.quantize_tensor(inp["w2"])
+    np.testing.assert_array_equal(host(g["w1"]), w1q)
+    np.testing.assert_array_equal(host(g["w2"]), w2q)
+    # A1 and A2 over the whole tensor, against the oracle's own norm and abs-max
+    r_ref, y_ref, rstd_ref, amax_y = oracle.residual_rmsnorm_absmax(inp["res"], inp["x"], inp["gain"], inp["eps"])
+    np.testing.assert_array_equal(bf(g["res_out"]), r_ref)
+    np.testing.assert_array_equal(bf(g["y"]), y_ref)
+    np.testing.assert_allclose(host(g["rstd"]), rstd_ref, rtol=2.0 ** -23, atol=0)
+    yq_ref, sy_ref = oracle.quantize_with_abs_max(y_ref, amax_y)
+    assert st[0] == amax_y and st[1] == sy_ref
+    yq = host(g["yq"])
+    np.testing.assert_array_equal(yq, yq_ref)
+    del r_ref, y_ref
+    # the abs-max of h: the GPU's equals the max of its own h and the oracle's own
+    # whole-tensor abs-max, bit for bit
+    assert st[2] == torch.max(torch.abs(g["h"].view(torch.bfloat16).float())).item()
+    amax_h, n_rows = oracle_whole_amax_h(q, g, yq, sy_ref, w1q, w1s, H)
+    assert st[2] == amax_h, (st[2], amax_h, n_rows)
+    assert st[3] == np.float32(amax_h / np.float32(448))
+    # sampled rows, stage by stage
+    h = bf(g["h"])[rows]
+    check_h_stage(q, g, yq[rows], h, st, w1q, w1s, H)
+    hq = host(g["hq"])[rows]
+    np.testing.assert_array_equal(hq, oracle.quantize_with_abs_max(h, st[2])[0])
+    out = bf(g["out"])[rows]
+    check_gemm_stage(out, hq, st[3], w2q, w2s)
+    # end to end on the sampled rows: the oracle's chain with its own abs-maxes
+    gu_ref = oracle.fp8_gemm_scaled(yq_ref[rows], sy_ref, w1q, w1s)
+    h_ref, _ = oracle.swiglu(gu_ref, H)
+    hq_ref, sh_ref = oracle.quantize_with_abs_max(h_ref, amax_h)
+    check_codes_rule(hq, hq_ref)
+    out_ref = oracle.fp8_gemm_scaled(hq_ref, sh_ref, w2q, w2s)
+    assert_out_close(out, out_ref)
+
+
 @pytest.mark.parametrize("name", ["tiny", "llama3.2-1b"])
 def test_forward_full_parity(q, name):
     check_full(q, PREFILL[name])
 
 
-def test_forward_qwen_outliers_full_parity(q):
+def _sample_rows(N, extra, seed=0):
+    return np.unique(np.concatenate([[0, 1, 127, 128, N // 2 - 1, N - 2, N - 1],
+                                     np.random.default_rng(seed).integers(0, N, extra)]))
+
+
+def test_forward_qwen_outliers_sampled(q):
     """Qwen2.5-7B shape, 0.1% outliers x20: stresses the abs-max scaling end to end."""
-    check_full(q, PREFILL["qwen2.5-7b"])
+    cfg = PREFILL["qwen2.5-7b"]
+    check_sampled(q, cfg, _sample_rows(cfg.N, 57))
 
 
 @pytest.mark.parametrize("B,T,C,H", [(1, 1, 128, 128), (3, 43, 256, 384), (1, 129, 384, 512),
@@ -171,37 +268,7 @@ def test_forward_repeatable(q):
 
 def test_forward_llama3_8b_sampled(q):
     """Full Llama-3-8B shape (N=16384, C=4096, H=14336) in the launch configuration the
-    benchmark times; sampled rows checked stage by stage, whole tensors by properties."""
+    benchmark times: whole-tensor A1/A2 and both abs-maxes against the oracle's own,
+    sampled rows stage by stage and end to end."""
     cfg = PREFILL["llama3-8b"]
-    inp = prefill_inputs(cfg)
-    g = run_forward(q, cfg, inp)
-    N = cfg.N
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, 8191, N - 2, N - 1],
-                                     np.random.default_rng(0).integers(0, N, 57)]))
-    st = host(g["stats"])
-    # whole-tensor abs-max properties (on the device)
-    assert st[0] == torch.max(torch.abs(g["y"].view(torch.bfloat16).float())).item()
-    assert st[2] == torch.max(torch.abs(g["h"].view(torch.bfloat16).float())).item()
-    assert st[1] == np.float32(st[0] / np.float32(448)) and st[3] == np.float32(st[2] / np.float32(448))
-    w1q, w1s = oracle.quantize_tensor(inp["w1"])
-    w2q, w2s = oracle.quantize_tensor(inp["w2"])
-    np.testing.assert_array_equal(host(g["w1"]), w1q)
-    np.testing.assert_array_equal(host(g["w2"]), w2q)
-    r, y_ref, rstd_ref, _ = oracle.residual_rmsnorm_absmax(inp["res"][rows], inp["x"][rows], inp["gain"], inp["eps"])
-    np.testing.assert_array_equal(bf(g["res_out"])[rows], r)
-    y = bf(g["y"])[rows]
-    np.testing.assert_array_equal(y, y_ref)
-    np.testing.assert_allclose(host(g["rstd"])[rows], rstd_ref, rtol=2.0 ** -23, atol=0)
-    yq = host(g["yq"])[rows]
-    np.testing.assert_array_equal(yq, oracle.quantize_with_abs_max(y, st[0])[0])
-    h = bf(g["h"])[rows]
-    check_h_stage(q, g, yq, h, st, w1q, w1s, cfg.H)
-    hq = host(g["hq"])[rows]
-    np.testing.assert_array_equal(hq, oracle.quantize_with_abs_max(h, st[2])[0])
-    out = bf(g["out"])[rows]
-    check_gemm_stage(out, hq, st[3], w2q, w2s)
-    # end to end on the sampled rows, the oracle chain using the oracle's own y rows
-    yq_ref = oracle.quantize_with_abs_max(y_ref, st[0])[0]
-    h_ref, _ = oracle.swiglu(oracle.fp8_gemm_scaled(yq_ref, st[1], w1q, w1s), cfg.H)
-    out_ref = oracle.fp8_gemm_scaled(oracle.quantize_with_abs_max(h_ref, st[2])[0], st[3], w2q, w2s)
-    assert_out_close(out, out_ref)
+    check_sampled(q, cfg, _sample_rows(cfg.N, 57))

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from ffn_inputs import random_bf16
-from gpu_util import bf, check_dot_outputs, dev, empty_bf16, empty_u8, host, sync
+from gpu_util import bf, check_dot_outputs, dev, empty_bf16, empty_u8, gemm_mismatch_bar, host, sync
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,10 @@ def test_qmm_parity(q, M, N, K, with_bias):
     np.testing.assert_array_equal(codes, rcodes)             # codes bit-exact
     absdot = (np.abs(oracle.e4m3_decode(rcodes)) @ np.abs(oracle.e4m3_decode(wq)).T) \
         * float(rscale) * float(ws)
-    check_dot_outputs(out, want, absdot, K, max_mismatch=2e-3)
+    exact = oracle.fp8_gemm_exact(rcodes, rscale, wq, ws)
+    if bias is not None:
+        exact = exact + oracle.bf16_to_f64(bias)[None, :]
+    check_dot_outputs(out, exact, absdot, K, gemm_mismatch_bar(K), want_bits=want)
 
 
 def test_qmm_bias_is_added_per_column(q):
@@ -92,4 +95,5 @@ def test_attention_qkv_projection_8b_sampled(q):
     assert st[1] == rscale
     np.testing.assert_array_equal(host(qbuf)[rows], rcodes)
     absdot = (np.abs(oracle.e4m3_decode(rcodes)) @ np.abs(oracle.e4m3_decode(wq)).T) * float(rscale) * float(ws)
-    check_dot_outputs(bf(out)[rows], want, absdot, C, max_mismatch=2e-3)
+    check_dot_outputs(bf(out)[rows], oracle.fp8_gemm_exact(rcodes, rscale, wq, ws), absdot, C, gemm_mismatch_bar(C),
+                      want_bits=want)

@@ -125,26 +125,3 @@ def test_bf16_single_rounding_from_f64_matches_brute_force():
 def test_bf16_decode_round_trip_all_finite():
     bits = np.array([b for b in range(65536) if ((b >> 7) & 0xFF) != 0xFF], dtype=np.uint16)
     np.testing.assert_array_equal(oracle.f64_to_bf16(oracle.bf16_to_f64(bits)), bits)
-
-
-@pytest.mark.parametrize("plant", ["half_away", "no_saturation"])
-def test_planted_e4m3_mistakes_are_caught(plant, monkeypatch):
-    """A plausible codec mistake planted in the oracle must fail the brute-force pin."""
-    import oracle.codecs as oc
-    real = oc.e4m3_encode
-
-    def half_away(v):
-        v = np.asarray(v, np.float64)
-        nudged = v + np.sign(v) * np.abs(v) * 1e-12          # breaks ties upward
-        return real(nudged)
-
-    def no_saturation(v):
-        v = np.asarray(v, np.float64)
-        c = real(v)
-        return np.where(np.abs(v) > 464, np.uint8(0x7F) | (c & 0x80), c).astype(np.uint8)
-
-    monkeypatch.setattr(oc, "e4m3_encode", half_away if plant == "half_away" else no_saturation)
-    with pytest.raises(AssertionError):
-        for val, code, _ in _rows("e4m3_rounding.txt"):
-            got = int(oc.e4m3_encode(np.array([float(val)]))[0])
-            assert got == int(code, 16)
