@@ -43,7 +43,7 @@ FP8_PER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor rate ratio
 # dram__bytes_write.sum).  Set to None whenever the kernel changes until it
 # is captured again.
 TRAFFIC_GATE_UP_BYTES = (1006.4 + 445.8) * 1e6
-TRAFFIC_DUAL_GEMV_BYTES = (117.6 + 0.1) * 1e6
+TRAFFIC_DUAL_GEMV_BYTES = None        # decode dual GEMV: not captured since its last change
 
 
 def load_peaks():
@@ -621,52 +621,72 @@ def bench_decode(q, torch, device, iters, dist, peaks):
         sets.append(s)
     x = to_dev(di["x"], torch, device)
     out = torch.empty(C, dtype=torch.int16, device=device)
-    ws = torch.empty(q.qffn_decode_workspace_size(C, H), dtype=torch.uint8, device=device)
+    ws = torch.zeros(q.qffn_decode_workspace_size(C, H), dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device)
-
-    def call(s):
-        q.qffn_decode_forward(out, x, *s["w_gate"], *s["w_up"], *s["w_down"], C, H, ws, stream=stream)
-
-    for i in range(6):
-        call(sets[i % copies])
     torch.cuda.synchronize()
-    # graph of one call per weight copy, replayed
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for s in sets:
-            call(s)
-    reps = max(1, iters // copies)
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    barrier(dist)
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for _ in range(reps):
+
+    def call(s, flags):
+        # a decode step on weights built long before: the weight stream may start
+        # before the previous step's kernel has finished
+        q.qffn_decode_forward_ex(out, x, *s["w_gate"], *s["w_up"], *s["w_down"], C, H, ws, flags,
+                                 stream=stream)
+
+    def graph_us(flags):
+        for i in range(6):
+            call(sets[i % copies], flags)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for s in sets:
+                call(s, flags)
+        reps = max(1, iters // copies)
+        for _ in range(3):
             graph.replay()
-        t1.record(stream)
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        barrier(dist)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(dist, t0.elapsed_time(t1)) * 1e3 / (reps * copies), reps * copies
+
+    stable = q.QFFN_DECODE_WEIGHTS_STABLE
+    us_graph, n_calls = graph_us(stable)
+    us_graph_default, _ = graph_us(0)
+
+    def eager_us(flags):
+        e_calls = max(1, iters // copies) * copies
+        for i in range(copies):
+            call(sets[i], flags)
+        torch.cuda.synchronize()
+        t2 = torch.cuda.Event(enable_timing=True)
+        t3 = torch.cuda.Event(enable_timing=True)
+        t2.record(stream)
+        for i in range(e_calls):
+            call(sets[i % copies], flags)
+        t3.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(dist, t2.elapsed_time(t3)) * 1e3 / e_calls
+
+    us_eager = eager_us(stable)
+    # one call between events (its two launches), each on a weight copy not in L2
+    kev = []
+    for i in range(60):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        e[0].record(stream)
+        call(sets[i % copies], 0)
+        e[1].record(stream)
+        kev.append(e)
     torch.cuda.synchronize()
-    n_calls = reps * copies
-    us_graph = max_over_ranks(dist, t0.elapsed_time(t1)) * 1e3 / n_calls
-    # the same calls launched eagerly back to back (each call's dual GEMV is a
-    # programmatic dependent launch of the previous call's down GEMV)
-    e_calls = reps * copies
-    for i in range(copies):
-        call(sets[i])
-    torch.cuda.synchronize()
-    t2 = torch.cuda.Event(enable_timing=True)
-    t3 = torch.cuda.Event(enable_timing=True)
-    t2.record(stream)
-    for i in range(e_calls):
-        call(sets[i % copies])
-    t3.record(stream)
-    torch.cuda.synchronize()
-    us_eager = max_over_ranks(dist, t2.elapsed_time(t3)) * 1e3 / e_calls
-    # ungraphed, with per-kernel events (dual GEMV is the dominant kernel)
-    g = ws[:2 * H].view(torch.int16)
-    u = ws[(2 * H + 255) // 256 * 256:].view(torch.int16)
+    call_us = statistics.mean(e[0].elapsed_time(e[1]) for e in kev[10:]) * 1e3
+    # the standalone kernels of the split arm, for context (dual GEMV, silu_mul, down GEMV)
+    g = torch.empty(H, dtype=torch.int16, device=device)
+    u = torch.empty(H, dtype=torch.int16, device=device)
+    o2 = torch.empty(C, dtype=torch.int16, device=device)
     evs = []
     for i in range(60):
         s = sets[i % copies]
@@ -676,31 +696,38 @@ def bench_decode(q, torch, device, iters, dist, peaks):
         e[1].record(stream)
         q.qffn_silu_mul(g, u, H, stream=stream)
         e[2].record(stream)
-        q.qffn_gemv(out, g, *s["w_down"], C, H, stream=stream)
+        q.qffn_gemv(o2, g, *s["w_down"], C, H, stream=stream)
         e[3].record(stream)
         evs.append(e)
     torch.cuda.synchronize()
+    q.qffn_check_status(stream)
     dual_us = statistics.mean(e[0].elapsed_time(e[1]) for e in evs[10:]) * 1e3
+    silu_us = statistics.mean(e[1].elapsed_time(e[2]) for e in evs[10:]) * 1e3
     down_us = statistics.mean(e[2].elapsed_time(e[3]) for e in evs[10:]) * 1e3
-    ungraphed_us = statistics.mean(e[0].elapsed_time(e[3]) for e in evs[10:]) * 1e3
-    dual_bytes = 2 * H * C + 8 * H + 2 * C + 4 * H
+    split_us = statistics.mean(e[0].elapsed_time(e[3]) for e in evs[10:]) * 1e3
     gbs = cfg.weight_bytes / (us_graph * 1e-6) / 1e9
+    dual_bytes = 2 * H * C + 8 * H + 2 * C + 4 * H
     dual_gbs = dual_bytes / (dual_us * 1e-6) / 1e9
     return {
         "metric": DECODE_METRIC, "unit": "GB/s", "value": gbs, "us_per_call": us_graph,
         "bytes_per_call": cfg.weight_bytes, "calls": n_calls, "graph": True,
-        "ungraphed_us_per_call": ungraphed_us, "weight_copies_rotated": copies,
+        "form": "qffn_decode_forward_ex with QFFN_DECODE_WEIGHTS_STABLE (weights built before the "
+                "timed region), a graph of one call per weight copy, replayed",
+        "default_form_us_per_call": us_graph_default,
+        "default_form_gbs": cfg.weight_bytes / (us_graph_default * 1e-6) / 1e9,
+        "weight_copies_rotated": copies,
         "eager_back_to_back_us_per_call": us_eager,
         "eager_back_to_back_gbs": cfg.weight_bytes / (us_eager * 1e-6) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<dual> (gate+up GEMV)",
+        "single_call_us": call_us,
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel<dual> (gate+up GEMV, the decode's first launch)",
                      "achieved": dual_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": dual_gbs / peaks["hbm_gbs"], "traffic": TRAFFIC_DUAL_GEMV_BYTES,
-                     "traffic_unit": "bytes per launch",
+                     "traffic_unit": "bytes per launch", "us_per_launch": dual_us,
                      "peak_note": f"{peaks['source']} HBM copy bandwidth"},
-        "stage_us": {"gemv_dual": dual_us, "gemv_down": down_us},
+        "split_arm_us": {"gemv_dual": dual_us, "silu_mul": silu_us, "gemv_down": down_us, "total": split_us},
         "frac_of_peak": gbs / peaks["hbm_gbs"],
         "frac_of_8tbs": gbs / 8000.0,
-        "gpu_launches": 2 * n_calls,        # dual GEMV (+silu_mul) and down GEMV, graph region
+        "gpu_launches": 2 * n_calls,        # dual GEMV (+silu_mul) and down GEMV per call, graph region
     }
 
 
@@ -845,7 +872,7 @@ def profile_case(q, torch, device):
     torch.cuda.empty_cache()
     x = to_dev(di["x"], torch, device)
     out = torch.empty(cfg.C, dtype=torch.int16, device=device)
-    ws = torch.empty(q.qffn_decode_workspace_size(cfg.C, cfg.H), dtype=torch.uint8, device=device)
+    ws = torch.zeros(q.qffn_decode_workspace_size(cfg.C, cfg.H), dtype=torch.uint8, device=device)
     for _ in range(2):
         q.qffn_decode_forward(out, x, *recs, cfg.C, cfg.H, ws, stream=stream)
     torch.cuda.synchronize()

@@ -363,19 +363,57 @@ qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream
 /* ---- Whole single-token decode FFN: A6 -> A7 -> A8 ------------------------
  * [metrale] DenseFfnLayer::forward, FP8 split-SiLU arm.  x [C] bf16 (already
  * normalised), Wg, Wu [H, C] E4M3 with s_gate, s_up [H]; Wd [C, H] E4M3 with
- * s_down [C]; out [C] bf16.  workspace >= qffn_decode_workspace_size() bytes,
- * 16-byte aligned.  After the call it holds, as the split-SiLU arm leaves
- * its buffers, h = bf16(silu(g) * u) [H] bf16 at offset 0 (the gate buffer)
- * and u [H] bf16 at offset round_up(2H, 256).  Two launches: the dual gate/up
- * GEMV with silu_mul applied as g and u are produced, then the down GEMV as a
- * programmatic dependent launch; bit-identical to qffn_gemv_dual,
- * qffn_silu_mul, qffn_gemv.
- * C % 16 == 0, H % 16 == 0, 16 <= C, H <= 32768. */
+ * s_down [C]; out [C] bf16.  C % 16 == 0, H % 16 == 0, 16 <= C, H <= 32768.
+ * workspace >= qffn_decode_workspace_size() bytes, 16-byte aligned, any
+ * content.  After the call it holds, as the split-SiLU arm leaves its
+ * buffers, h = bf16(silu(g) * u) [H] bf16 (the gate buffer) and u [H] bf16
+ * at the byte offsets qffn_decode_workspace_offsets() returns (0 and
+ * round_up(2H, 256)).  Two launches: the dual gate/up GEMV with silu_mul
+ * applied as g and u are produced, then the down GEMV as a programmatic
+ * dependent launch; bit-identical to qffn_gemv_dual, qffn_silu_mul,
+ * qffn_gemv.
+ *
+ * Ordering: both launches are programmatic dependent launches.  The down
+ * GEMV starts streaming w_down before the dual GEMV has finished (it waits
+ * only for h), which is always safe: it cannot start before the work that
+ * preceded the call has finished.  Without QFFN_DECODE_WEIGHTS_STABLE the
+ * dual GEMV reads nothing before the preceding work on the stream has
+ * finished. */
 size_t qffn_decode_workspace_size(int64_t C, int64_t H);
+qffn_status qffn_decode_workspace_offsets(int64_t C, int64_t H, size_t offsets[2] /* h, u */);
 qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
                                 const float* s_gate, const uint8_t* w_up, const float* s_up,
                                 const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
                                 void* workspace, size_t workspace_bytes, qffn_stream_t stream);
+
+/* qffn_decode_forward with flags.
+ * QFFN_DECODE_WEIGHTS_STABLE: the dual GEMV starts streaming w_gate and w_up
+ * (not x, the row scales or the workspace) before the kernel enqueued just
+ * before this call on the stream has finished, so the weight stream of a
+ * decode step overlaps the end of the previous one.  Set it only when no
+ * work that can still be running at that point writes those weights: not
+ * the kernel just before this call (for example qffn_quantize_rows building
+ * them), nor, when that kernel is itself a programmatic dependent launch,
+ * the kernels it may overlap.  Weights written before a stream or event
+ * synchronisation, or before an ordinary (non-programmatic) launch that
+ * precedes this call on the stream, are safe.  Unknown flag bits give
+ * QFFN_ERR_INVALID_ARG. */
+#define QFFN_DECODE_WEIGHTS_STABLE 1u
+qffn_status qffn_decode_forward_ex(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
+                                   const float* s_gate, const uint8_t* w_up, const float* s_up,
+                                   const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
+                                   void* workspace, size_t workspace_bytes, unsigned int flags,
+                                   qffn_stream_t stream);
+
+/* The decode with the gate and up weights as one fused record, the layout
+ * of the fused up projection (R1: gate rows first): w_gu [2H, C] E4M3 (rows
+ * [0, H) gate, [H, 2H) up) with gu_row_scale [2H] fp32.  Forwards to
+ * qffn_decode_forward with w_gate = w_gu, w_up = w_gu + H*C,
+ * s_gate = gu_row_scale, s_up = gu_row_scale + H; the same rules apply. */
+qffn_status qffn_decode_forward_gu(uint16_t* out, const uint16_t* x, const uint8_t* w_gu,
+                                   const float* gu_row_scale, const uint8_t* w_down,
+                                   const float* s_down, int64_t C, int64_t H, void* workspace,
+                                   size_t workspace_bytes, qffn_stream_t stream);
 
 /* ---- Decode FFN without a caller workspace ---------------------------------
  * The pages have no counterpart of this call; it exists for callers that
@@ -386,15 +424,16 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
  * Computes exactly what qffn_decode_forward computes (same kernels, same
  * bits), with its scratch (the g and u vectors) in a fixed array inside the
  * library: 2 x 32768 bf16 (128 KiB) per GPU that loads the library, held
- * until the process exits.  H > 32768 is rejected with
+ * until the process exits.  H > 32768 (and C > 32768) is rejected with
  * QFFN_ERR_UNSUPPORTED_SHAPE; the other size and alignment rules are those of
  * qffn_decode_forward.  Nothing is allocated by this call.
- * The first call on each device looks up the array's device address (with
- * that device current); make that first call before any stream capture.
- * All calls on a device share the array and it keeps the last call's
- * contents (g and u are written before they are read, so nothing needs
- * clearing).  Calls that overlap in time on the GPU race on the array: order
- * them on one stream or with events. */
+ * The first call with a given current CUDA context looks up the array's
+ * device address in that context (after cudaDeviceReset, or under another
+ * context, it is looked up again); make that first call before any stream
+ * capture.  All calls on a device share the array and it keeps the last
+ * call's contents (g and u are written before they are read, so nothing
+ * needs clearing).  Calls that overlap in time on the GPU race on the
+ * array: order them on one stream or with events. */
 qffn_status qffn_decode_forward_noalloc(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
                                         const float* s_gate, const uint8_t* w_up,
                                         const float* s_up, const uint8_t* w_down,

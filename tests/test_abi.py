@@ -129,6 +129,20 @@ def test_decode_checks(lib):
     assert _call(lib, "qffn_quantize_rows", A, A, A, 3, 8, None) == 2
 
 
+def test_decode_variant_checks(lib):
+    ws = lib.qffn_decode_workspace_size(4096, 14336)
+    assert ws >= 2 * 2 * 14336                                      # g (then h) and u
+    ex = lambda *a: _call(lib, "qffn_decode_forward_ex", *a)
+    good = [A, A, A, A, A, A, A, A, 4096, 14336, A, ws]
+    assert ex(*good, 2, None) == 1                                   # unknown flag bit
+    assert ex(*good[:10], A, ws - 1, 1, None) == 1                  # workspace too small
+    assert ex(*good[:10], A + 8, ws, 1, None) == 3                  # workspace alignment
+    gu = lambda *a: _call(lib, "qffn_decode_forward_gu", *a)
+    assert gu(A, A, NULL, A, A, A, 4096, 14336, A, ws, None) == 1
+    assert gu(A, A, A, A, A, A, 4096, 14330, A, ws, None) == 2
+    assert gu(A, A, A, A + 2, A, A, 4096, 14336, A, ws, None) == 3  # gu_row_scale
+
+
 def test_python_binding_raises(lib):
     with pytest.raises(lib.QffnError) as e:
         lib.qffn_gemv(A, A, A, A, 10, 24, stream=0)
@@ -230,6 +244,7 @@ def test_decode_noalloc_argument_checks(lib):
         assert f(*bad) == 1, i
     assert f(A, A, A, A, A, A, A, A, 24, 768, None) == 2      # C % 16
     assert f(A, A, A, A, A, A, A, A, 256, 32784, None) == 2   # H above the library's scratch
+    assert f(A, A, A, A, A, A, A, A, 32784, 256, None) == 2   # C above the library's scratch
     assert f(A, MIS, A, A, A, A, A, A, 256, 768, None) == 3   # x
     assert f(A, A, A, A + 2, A, A, A, A, 256, 768, None) == 3  # s_gate
 

@@ -123,6 +123,9 @@ def test_decode_outputs_stay_inside(q):
         codes, scales = oracle.quantize_rows(random_bf16((rows, cols), seed=seed, std=0.02))
         recs += [dev(codes), dev(scales)]
     out = Guarded(C * 2)
-    ws = torch.empty(q.qffn_decode_workspace_size(C, H), dtype=torch.uint8, device="cuda")
-    q.qffn_decode_forward(out.view(torch.int16, C), x, *recs, C, H, ws)
+    ws_bytes = q.qffn_decode_workspace_size(C, H)
+    ws = Guarded(ws_bytes)                          # the workspace must stay inside its bytes too
+    ws.view(torch.uint8, ws_bytes).zero_()
+    q.qffn_decode_forward(out.view(torch.int16, C), x, *recs, C, H, ws.view(torch.uint8, ws_bytes))
     out.check("decode out")
+    ws.check("decode workspace")

@@ -22,13 +22,16 @@ def _records(q, w_bits):
     return codes, scales
 
 
-@pytest.mark.parametrize("C,H", [(4096, 14336), (256, 768)])
+@pytest.mark.parametrize("C,H", [(4096, 14336), (256, 768),
+                                 # the largest sizes the fixed scratch holds: h and u end at its
+                                 # end at H = 32768, the slice partials at C = 32768
+                                 (64, 32768), (32768, 64)])
 def test_noalloc_decode_matches_workspace_decode_twice(C, H):
     import transformer_ffn_block_gb300 as q
     cfg = DecodeConfig("noalloc", C=C, H=H, seed=C + H)
     di = decode_inputs(cfg)
     recs = [t for k in ("w_gate", "w_up", "w_down") for t in _records(q, di[k])]
-    ws = torch.empty(q.qffn_decode_workspace_size(C, H), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(q.qffn_decode_workspace_size(C, H), dtype=torch.uint8, device="cuda")
     g = torch.Generator().manual_seed(7)
     xs = [torch.from_numpy(di["x"]).view(torch.int16).cuda(),
           (torch.randn(C, generator=g)).to(torch.bfloat16).view(torch.int16).cuda()]

@@ -26,8 +26,11 @@ __all__ = [
     "qffn_backward_qmm_workspace_size", "qffn_backward_qmm", "qffn_ffn_backward_workspace_size",
     "qffn_ffn_backward_workspace_offsets", "qffn_ffn_backward", "qffn_gate_up_swiglu_backward",
     "qffn_gemv_dual", "qffn_gemv", "qffn_gemv_silu_input", "qffn_silu_mul", "qffn_decode_workspace_size",
-    "qffn_decode_forward", "qffn_decode_forward_noalloc",
+    "qffn_decode_workspace_offsets", "qffn_decode_forward", "qffn_decode_forward_ex", "qffn_decode_forward_gu",
+    "qffn_decode_forward_noalloc", "QFFN_DECODE_WEIGHTS_STABLE",
 ]
+
+QFFN_DECODE_WEIGHTS_STABLE = 1
 
 STATUS = {0: "QFFN_OK", 1: "QFFN_ERR_INVALID_ARG", 2: "QFFN_ERR_UNSUPPORTED_SHAPE",
           3: "QFFN_ERR_MISALIGNED", 4: "QFFN_ERR_CUDA", 5: "QFFN_ERR_TIMEOUT"}
@@ -80,7 +83,10 @@ _SIGS = {
     "qffn_gemv_silu_input": ([_P, _P, _P, _P, _P, _I64, _I64, _P], _S),
     "qffn_silu_mul": ([_P, _P, _I64, _P], _S),
     "qffn_decode_workspace_size": ([_I64, _I64], _SZ),
+    "qffn_decode_workspace_offsets": ([_I64, _I64, _P], _S),
     "qffn_decode_forward": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P], _S),
+    "qffn_decode_forward_ex": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, ctypes.c_uint, _P], _S),
+    "qffn_decode_forward_gu": ([_P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P], _S),
     "qffn_decode_forward_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P], _S),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -299,6 +305,13 @@ def qffn_decode_workspace_size(C, H) -> int:
     return int(lib.qffn_decode_workspace_size(int(C), int(H)))
 
 
+def qffn_decode_workspace_offsets(C, H):
+    """Byte offsets of h and u in the decode workspace."""
+    off = (ctypes.c_size_t * 2)()
+    _check("qffn_decode_workspace_offsets", lib.qffn_decode_workspace_offsets(int(C), int(H), off))
+    return [int(off[0]), int(off[1])]
+
+
 def qffn_decode_forward(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, workspace,
                         workspace_bytes=None, stream=None):
     if workspace_bytes is None:
@@ -308,10 +321,28 @@ def qffn_decode_forward(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H
         _ptr(s_down), int(C), int(H), _ptr(workspace), int(workspace_bytes), _stream(stream)))
 
 
+def qffn_decode_forward_ex(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, workspace, flags,
+                           workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("qffn_decode_forward_ex", lib.qffn_decode_forward_ex(
+        _ptr(out), _ptr(x), _ptr(w_gate), _ptr(s_gate), _ptr(w_up), _ptr(s_up), _ptr(w_down),
+        _ptr(s_down), int(C), int(H), _ptr(workspace), int(workspace_bytes), int(flags), _stream(stream)))
+
+
+def qffn_decode_forward_gu(out, x, w_gu, gu_row_scale, w_down, s_down, C, H, workspace,
+                           workspace_bytes=None, stream=None):
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    _check("qffn_decode_forward_gu", lib.qffn_decode_forward_gu(
+        _ptr(out), _ptr(x), _ptr(w_gu), _ptr(gu_row_scale), _ptr(w_down), _ptr(s_down), int(C), int(H),
+        _ptr(workspace), int(workspace_bytes), _stream(stream)))
+
+
 def qffn_decode_forward_noalloc(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H,
                                 stream=None):
-    """qffn_decode_forward for callers that cannot allocate: the g/u scratch is a fixed
-    array inside the library (H <= 32768); calls overlapping on the GPU race on it."""
+    """qffn_decode_forward for callers that cannot allocate: the scratch is a fixed array
+    inside the library (C, H <= 32768); calls overlapping on the GPU race on it."""
     _check("qffn_decode_forward_noalloc", lib.qffn_decode_forward_noalloc(
         _ptr(out), _ptr(x), _ptr(w_gate), _ptr(s_gate), _ptr(w_up), _ptr(s_up), _ptr(w_down),
         _ptr(s_down), int(C), int(H), _stream(stream)))

@@ -109,10 +109,13 @@ cudaError_t run_backward_qmm(uint16_t* dinp, uint16_t* dw, float* stats_dout, co
                                 accumulate, true, true);
 }
 
-// decode workspace: g [H] bf16 | u [H] bf16, each 256-byte aligned
-void decode_offsets(int64_t H, size_t off[2]) {
-  off[0] = round_up(size_t(H) * 2, 256);   // u
-  off[1] = 2 * off[0];                     // end
+// decode workspace: g [H] bf16 (holds h after the call) | u [H] bf16, each
+// 256-byte aligned
+void decode_offsets(int64_t H, size_t off[3]) {
+  const size_t vec = round_up(size_t(H) * 2, 256);
+  off[0] = 0;                                  // g, then h
+  off[1] = vec;                                // u
+  off[2] = 2 * vec;                            // end
 }
 
 qffn_status check_forward_shape(int64_t B, int64_t T, int64_t C, int64_t H) {
@@ -565,18 +568,30 @@ qffn_status qffn_silu_mul(uint16_t* g, const uint16_t* u, int64_t n, qffn_stream
 
 size_t qffn_decode_workspace_size(int64_t C, int64_t H) {
   if (C < 16 || H < 16 || C > 32768 || H > 32768) return 0;
-  size_t off[2];
+  size_t off[3];
   decode_offsets(H, off);
-  return off[1];
+  return off[2];
 }
 
-qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
-                                const float* s_gate, const uint8_t* w_up, const float* s_up,
-                                const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
-                                void* workspace, size_t workspace_bytes, qffn_stream_t stream) {
+qffn_status qffn_decode_workspace_offsets(int64_t C, int64_t H, size_t offsets[2]) {
+  QFFN_PTR(offsets);
+  QFFN_REQUIRE(C >= 16 && H >= 16 && C <= 32768 && H <= 32768, QFFN_ERR_UNSUPPORTED_SHAPE);
+  size_t off[3];
+  decode_offsets(H, off);
+  offsets[0] = off[0];
+  offsets[1] = off[1];
+  return QFFN_OK;
+}
+
+qffn_status qffn_decode_forward_ex(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
+                                   const float* s_gate, const uint8_t* w_up, const float* s_up,
+                                   const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
+                                   void* workspace, size_t workspace_bytes, unsigned int flags,
+                                   qffn_stream_t stream) {
   QFFN_RANGE();
   QFFN_PTR(out); QFFN_PTR(x); QFFN_PTR(w_gate); QFFN_PTR(s_gate); QFFN_PTR(w_up); QFFN_PTR(s_up);
   QFFN_PTR(w_down); QFFN_PTR(s_down); QFFN_PTR(workspace);
+  QFFN_REQUIRE((flags & ~QFFN_DECODE_WEIGHTS_STABLE) == 0u, QFFN_ERR_INVALID_ARG);
   QFFN_REQUIRE(C % 16 == 0 && H % 16 == 0 && C >= 16 && H >= 16 && C <= 32768 && H <= 32768,
                QFFN_ERR_UNSUPPORTED_SHAPE);
   QFFN_REQUIRE(workspace_bytes >= qffn_decode_workspace_size(C, H), QFFN_ERR_INVALID_ARG);
@@ -584,13 +599,32 @@ qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t*
   QFFN_ALIGNED4(s_gate); QFFN_ALIGNED4(s_up); QFFN_ALIGNED4(s_down);
   QFFN_ALIGNED(workspace);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  size_t off[2];
+  size_t off[3];
   decode_offsets(H, off);
-  uint16_t* g = reinterpret_cast<uint16_t*>(ws);
-  uint16_t* u = reinterpret_cast<uint16_t*>(ws + off[0]);
-  // A6, then A7 folded into A8 (see decode.cu)
-  return from_cuda(qffn::launch_decode(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, g,
-                                       u, stream));
+  // A6 with A7 folded into its output, then A8 (see decode.cu)
+  return from_cuda(qffn::launch_decode(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H,
+                                       reinterpret_cast<uint16_t*>(ws + off[0]),
+                                       reinterpret_cast<uint16_t*>(ws + off[1]),
+                                       (flags & QFFN_DECODE_WEIGHTS_STABLE) != 0u, stream));
+}
+
+qffn_status qffn_decode_forward(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
+                                const float* s_gate, const uint8_t* w_up, const float* s_up,
+                                const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
+                                void* workspace, size_t workspace_bytes, qffn_stream_t stream) {
+  return qffn_decode_forward_ex(out, x, w_gate, s_gate, w_up, s_up, w_down, s_down, C, H, workspace,
+                                workspace_bytes, 0u, stream);
+}
+
+qffn_status qffn_decode_forward_gu(uint16_t* out, const uint16_t* x, const uint8_t* w_gu,
+                                   const float* gu_row_scale, const uint8_t* w_down,
+                                   const float* s_down, int64_t C, int64_t H, void* workspace,
+                                   size_t workspace_bytes, qffn_stream_t stream) {
+  QFFN_PTR(w_gu); QFFN_PTR(gu_row_scale);
+  QFFN_REQUIRE(C >= 0 && H >= 0 && C <= 32768 && H <= 32768, QFFN_ERR_UNSUPPORTED_SHAPE);
+  return qffn_decode_forward_ex(out, x, w_gu, gu_row_scale, w_gu + size_t(H) * size_t(C),
+                                gu_row_scale + H, w_down, s_down, C, H, workspace, workspace_bytes,
+                                0u, stream);
 }
 
 }  // extern "C"

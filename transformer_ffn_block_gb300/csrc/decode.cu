@@ -29,9 +29,10 @@
 // leaves h = bf16(silu(g) * u) in the gate buffer (the split-SiLU arm's
 // buffer use); the down GEMV on h is a programmatic dependent launch whose
 // CTAs start as the dual GEMV's CTAs retire and wait for h only right before
-// reading it.  Each GEMV issues its first weight loads before that wait, and
-// the decode's dual GEMV is itself a programmatic dependent launch, so weight
-// streaming starts while the preceding kernel on the stream drains.
+// reading it, its first weight loads issued before that wait.  The dual GEMV
+// is itself a programmatic dependent launch; it issues its first weight loads
+// before waiting for the preceding kernel only when the caller states that
+// the weights are not being written by work that may still be running.
 #include "common.cuh"
 #include "launch.h"
 
@@ -75,7 +76,7 @@ struct Gemv {
 // instead of g -- the decode's silu_mul applied where g and u are produced,
 // as the split-SiLU arm leaves h in the gate buffer.
 template <bool DUAL, bool SILU, int TPR, bool SILU_IN = false>
-__global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
+__global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G, const bool early) {
   constexpr int kU = DUAL ? kUDual : kUSingle;
   extern __shared__ uint4 xs[];
   __shared__ float red[2][kThreads / 32];
@@ -87,11 +88,11 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = threadIdx.x / TPR, t = threadIdx.x % TPR;
 
-  // The weights do not depend on the preceding kernel: each team issues the
-  // first batch of its first row before waiting for x.
+  // The weights do not depend on the preceding kernel: with `early`, each team
+  // issues the first batch of its first row before waiting for x.
   uint4 a[kU], b[kU];
   bool have = false;
-  {
+  if (early) {
     const int row = blockIdx.x * RPB + sub;
     if (row < rows) {
       const uint8_t* r0 = G.w[0] + size_t(row) * size_t(cols);
@@ -207,7 +208,7 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(const Gemv G) {
 }
 
 template <bool DUAL, bool SILU, int TPR, bool SILU_IN = false>
-cudaError_t launch_t(const Gemv& G, bool pdl, cudaStream_t s) {
+cudaError_t launch_t(const Gemv& G, bool pdl, bool early, cudaStream_t s) {
   const size_t smem = size_t(G.cols) * 2;
   auto fn = gemv_kernel<DUAL, SILU, TPR, SILU_IN>;
   if (smem > 48 * 1024) {
@@ -231,14 +232,14 @@ cudaError_t launch_t(const Gemv& G, bool pdl, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, fn, G);
+  return cudaLaunchKernelEx(&cfg, fn, G, early);
 }
 
 template <bool DUAL, bool SILU>
-cudaError_t launch_d(const Gemv& G, bool pdl, cudaStream_t s) {
+cudaError_t launch_d(const Gemv& G, bool pdl, bool early, cudaStream_t s) {
   // one warp per row at every row length: the memory system is kept busy by
   // the number of rows in flight, and no cross-warp sums are needed
-  return launch_t<DUAL, SILU, 32>(G, pdl, s);
+  return launch_t<DUAL, SILU, 32>(G, pdl, early, s);
 }
 
 }  // namespace
@@ -257,7 +258,8 @@ cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const
   G.s[1] = s1;
   G.rows = int(rows);
   G.cols = int(cols);
-  return w1 != nullptr ? launch_d<true, false>(G, pdl, s) : launch_d<false, false>(G, pdl, s);
+  // standalone, or behind this library's own dual GEMV: the weights may be read early
+  return w1 != nullptr ? launch_d<true, false>(G, pdl, true, s) : launch_d<false, false>(G, pdl, true, s);
 }
 
 cudaError_t launch_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint16_t* u,
@@ -272,13 +274,13 @@ cudaError_t launch_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint1
   G.s[0] = row_scale;
   G.rows = int(rows);
   G.cols = int(cols);
-  return launch_t<false, false, 32, true>(G, false, s);
+  return launch_t<false, false, 32, true>(G, false, true, s);
 }
 
 cudaError_t launch_decode(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
                           const float* s_gate, const uint8_t* w_up, const float* s_up,
                           const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
-                          uint16_t* g, uint16_t* u, cudaStream_t s) {
+                          uint16_t* g, uint16_t* u, bool early, cudaStream_t s) {
   Gemv G{};
   G.out[0] = g;                      // receives h = bf16(silu(g) * u)
   G.out[1] = u;
@@ -289,7 +291,11 @@ cudaError_t launch_decode(uint16_t* out, const uint16_t* x, const uint8_t* w_gat
   G.s[1] = s_up;
   G.rows = int(H);
   G.cols = int(C);
-  cudaError_t e = launch_d<true, true>(G, true, s);
+  // the dual GEMV reads its weights before the preceding kernel has finished
+  // only when the caller allows it (`early`); the down GEMV's launch can start
+  // only once every dual CTA has passed its own wait, so whatever preceded the
+  // call has finished by then and its early weight loads are always safe
+  cudaError_t e = launch_d<true, true>(G, true, early, s);
   if (e != cudaSuccess) return e;
   return launch_gemv(out, nullptr, g, w_down, s_down, nullptr, nullptr, C, H, true, s);
 }

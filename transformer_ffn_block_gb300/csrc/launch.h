@@ -83,6 +83,8 @@ cudaError_t launch_swiglu_backward(uint16_t* dgu, float* stats, const uint16_t* 
 
 // ---- decode GEMVs (decode.cu)
 // out0[r] = bf16(s0[r] * W0[r,:] . x); with W1 != NULL also out1 from W1, s1.
+// With `pdl` the launch is a programmatic dependent launch that issues its
+// first weight loads before waiting for the preceding kernel.
 cudaError_t launch_gemv(uint16_t* out0, uint16_t* out1, const uint16_t* x, const uint8_t* w0,
                         const float* s0, const uint8_t* w1, const float* s1, int64_t rows,
                         int64_t cols, bool pdl, cudaStream_t s);
@@ -94,11 +96,13 @@ cudaError_t launch_gemv_silu_input(uint16_t* out, const uint16_t* g, const uint1
 // The whole decode FFN: the dual GEMV (g, u), then the down GEMV on
 // h = bf16(silu(g) * u) formed in its prologue, launched as a programmatic
 // dependent launch so its first weight loads overlap the dual GEMV's tail.
-// Same bits as launch_gemv + launch_silu_mul + launch_gemv.
+// `early`: the dual GEMV may read w_gate and w_up before the preceding kernel
+// on the stream has finished.  Same bits as launch_gemv + launch_silu_mul +
+// launch_gemv.
 cudaError_t launch_decode(uint16_t* out, const uint16_t* x, const uint8_t* w_gate,
                           const float* s_gate, const uint8_t* w_up, const float* s_up,
                           const uint8_t* w_down, const float* s_down, int64_t C, int64_t H,
-                          uint16_t* g, uint16_t* u, cudaStream_t s);
+                          uint16_t* g, uint16_t* u, bool early, cudaStream_t s);
 // Reads and clears the decode kernels' device status word of the current device.
 cudaError_t decode_take_status(unsigned int* status);
 
