@@ -42,8 +42,8 @@ FP8_PER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor rate ratio
 # capture of this benchmark's full-size workload (dram__bytes_read.sum +
 # dram__bytes_write.sum).  Set to None whenever the kernel changes until it
 # is captured again.
-TRAFFIC_GATE_UP_BYTES = (1006.4 + 445.8) * 1e6
-TRAFFIC_DUAL_GEMV_BYTES = None        # decode dual GEMV: not captured since its last change
+TRAFFIC_GATE_UP_BYTES = (817.4 + 449.2) * 1e6
+TRAFFIC_DUAL_GEMV_BYTES = (117.6 + 0.1) * 1e6
 
 
 def load_peaks():
@@ -879,6 +879,45 @@ def profile_case(q, torch, device):
     print("profile case done")
 
 
+def traffic_case(q, torch, device):
+    """A case for one ncu capture of DRAM bytes per launch (about 1.2 GB on the device):
+    the gate|up GEMM with the SwiGLU epilogue and the down GEMM at the 8B prefill shape
+    (N=16384, C=4096, H=14336) twice each on random codes, then two 8B decode calls.
+    Launch order: gate|up, down, gate|up, down, then per decode call the dual GEMV and
+    the down GEMV."""
+    cfg = PREFILL_CFG
+    N, C, H = cfg.N, cfg.C, cfg.H
+    g = torch.Generator(device=device).manual_seed(0)
+    yq = torch.randint(0, 0x70, (N, C), dtype=torch.uint8, device=device, generator=g)
+    w1 = torch.randint(0, 0x70, (2 * H, C), dtype=torch.uint8, device=device, generator=g)
+    hq = torch.randint(0, 0x70, (N, H), dtype=torch.uint8, device=device, generator=g)
+    w2 = torch.randint(0, 0x70, (C, H), dtype=torch.uint8, device=device, generator=g)
+    sc = torch.tensor([1e-3, 1e-3], dtype=torch.float32, device=device)
+    h = torch.empty(N, H, dtype=torch.int16, device=device)
+    out = torch.empty(N, C, dtype=torch.int16, device=device)
+    st = torch.zeros(2, dtype=torch.float32, device=device)
+    for _ in range(2):
+        q.qffn_gate_up_swiglu(h, st, yq, sc[0:1], w1, sc[1:2], N, C, H)
+        q.qffn_fp8_gemm_scaled(out, hq, sc[0:1], w2, sc[1:2], N, C, H)
+    torch.cuda.synchronize()
+    del yq, w1, hq, w2, h, out
+    dc = DECODE_CFG
+    di = decode_inputs(dc)
+    recs = []
+    for k, rows, cols in (("w_gate", dc.H, dc.C), ("w_up", dc.H, dc.C), ("w_down", dc.C, dc.H)):
+        codes = torch.empty(rows, cols, dtype=torch.uint8, device=device)
+        scales = torch.empty(rows, dtype=torch.float32, device=device)
+        q.qffn_quantize_rows(codes, scales, to_dev(di[k], torch, device), rows, cols)
+        recs += [codes, scales]
+    x = to_dev(di["x"], torch, device)
+    o = torch.empty(dc.C, dtype=torch.int16, device=device)
+    ws = torch.empty(q.qffn_decode_workspace_size(dc.C, dc.H), dtype=torch.uint8, device=device)
+    for _ in range(2):
+        q.qffn_decode_forward(o, x, *recs, dc.C, dc.H, ws)
+    torch.cuda.synchronize()
+    print("traffic case done")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -889,6 +928,8 @@ def main():
     ap.add_argument("--decode-iters", type=int, default=300)
     ap.add_argument("--profile-case", action="store_true",
                     help="run a small case once (for ncu captures) and exit without timing")
+    ap.add_argument("--traffic-case", action="store_true",
+                    help="run the full-size GEMMs and decode twice (for an ncu DRAM-bytes capture) and exit")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -903,6 +944,9 @@ def main():
     torch.cuda.set_device(device)
     if args.profile_case:
         profile_case(q, torch, device)
+        return
+    if args.traffic_case:
+        traffic_case(q, torch, device)
         return
     peaks = load_peaks()
     pre = bench_prefill(q, torch, device, args.steps, args.warmup, dist, peaks)

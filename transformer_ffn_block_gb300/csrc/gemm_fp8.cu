@@ -90,6 +90,8 @@ constexpr int STAGING_BYTES = 4 * 2 * STAGE_BOX_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + NUM_BARS * 8 + 16;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 constexpr int GROUP_M = 8;     // tile raster: 8 pair M-blocks (2048 rows) sweep the N-blocks together
+                                // (16, 32 and 64 measured: more DRAM reads or slower; one, N-fastest: the
+                                // down GEMM's 58.7 MB weight matrix is not kept in L2 either)
 constexpr uint16_t kBothCtas = 0x3;
 constexpr uint16_t kLeaderOnly = 0x1;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
@@ -317,7 +319,11 @@ QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
   const int gsize = min(a.tiles_m - first_m, GROUP_M);
   const int r = tile - group * per_group;
   mb = first_m + r % gsize;
-  nb = r / gsize;
+  // serpentine: odd groups sweep the N-blocks backwards, so a group starts on
+  // the weight slices the previous group read last (still in L2).  Measured at
+  // the 8B shape (ncu DRAM bytes per launch): gate|up reads 1006 -> 816 MB,
+  // down 1019 -> 920 MB, same time.
+  nb = (group & 1) ? a.tiles_n - 1 - r / gsize : r / gsize;
 }
 
 template <int EPI, bool A_MN = false, bool B_MN = false>
