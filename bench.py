@@ -52,7 +52,7 @@ def load_peaks():
         with open(path) as f:
             p = json.load(f)
         return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
-                "source": "measured"}
+                "sm_max_mhz": float(p.get("sm_max_mhz", 0.0)) or None, "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
@@ -574,6 +574,27 @@ def bench_backward(q, torch, device, steps, warmup, peaks):
     }
 
 
+# Dense FP8 (E4M3, kind::f8f6f4) tensor-core rate per SM per clock: twice the
+# dense BF16 rate of 8192 FLOP/clk/SM.  The nominal 4.5 PFLOP/s dense FP8 of a
+# 152-SM part corresponds to this rate at about 1.81 GHz.
+FP8_FLOP_PER_CLK_PER_SM = 16384
+
+
+def fp8_peak_computed(torch, device, clocks, peaks):
+    """SMs x SM clock x per-SM dense FP8 rate, reported beside the measured
+    ceilings: at the SM clock seen under load in the timed region and at the
+    part's maximum clock."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    out = {"sms": sms, "flop_per_clk_per_sm": FP8_FLOP_PER_CLK_PER_SM,
+           "note": "dense FP8 rate per SM per clock (2 x the BF16 rate); the nominal 4.5 PFLOP/s "
+                   "corresponds to it at about 1.81 GHz"}
+    for key, mhz in (("at_max_clock", clocks.get("sm_max_mhz") or peaks.get("sm_max_mhz")),
+                     ("at_clock_under_load", clocks.get("sm_mhz"))):
+        if mhz:
+            out[key] = {"sm_mhz": mhz, "tflops": sms * mhz * 1e6 * FP8_FLOP_PER_CLK_PER_SM / 1e12}
+    return out
+
+
 def fp8_library_ceiling(torch, device, steps=10):
     """Context only, not on the library's path: the FP8 rate of the vendor GEMM
     (cuBLASLt through torch._scaled_mm, E4M3 x E4M3 -> bf16, per-tensor
@@ -954,6 +975,7 @@ def main():
     att = bench_attention_projections(q, torch, device, args.steps, args.warmup)
     bwd = bench_backward(q, torch, device, max(3, args.steps // 4), args.warmup, peaks)
     ceiling = fp8_library_ceiling(torch, device)
+    computed = fp8_peak_computed(torch, device, pre["clocks"], peaks)
     workloads = {name: bench_workload(q, torch, device, PREFILL[name], max(5, args.steps // 2), args.warmup, peaks)
                  for name in ("tiny", "llama3.2-1b", "qwen2.5-7b")}
     cfg = PREFILL_CFG
@@ -979,6 +1001,7 @@ def main():
         "attention_projections": att,
         "backward": bwd,
         "fp8_library_ceiling": ceiling,
+        "fp8_peak_computed": computed,
         "decode": dec,
         "workloads": workloads,
     }
