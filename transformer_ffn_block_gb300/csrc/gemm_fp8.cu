@@ -89,7 +89,7 @@ constexpr int STAGE_BOX_BYTES = 32 * 64 * 2;
 constexpr int STAGING_BYTES = 4 * 2 * STAGE_BOX_BYTES;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STAGING_BYTES + 1024 + NUM_BARS * 8 + 16;
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
-constexpr int GROUP_M = 8;     // tile raster: 8 pair M-blocks (2048 rows) sweep the N-blocks together
+constexpr int GROUP_M = 8;     // tile raster: 8 pair M-blocks (2048 rows) sweep a band of N-blocks together
                                 // (16, 32 and 64 measured: more DRAM reads or slower; one, N-fastest: the
                                 // down GEMM's 58.7 MB weight matrix is not kept in L2 either)
 constexpr uint16_t kBothCtas = 0x3;
@@ -133,6 +133,7 @@ struct GemmArgs {
   int M, N, K;   // N: output columns (SwiGLU: H)
   int H;         // SwiGLU: first up row of W1
   int tiles_m, tiles_n, num_tiles, num_kb;
+  int band_n;    // N-blocks per raster band (tile_coords)
   // Work units below split_from are 256-column tiles; each unit from there on
   // is one 128-column half of the tiles split_from, split_from + 1, ...:
   // a last partial wave of R tiles runs as 2R half tiles in half the time
@@ -312,18 +313,25 @@ QFFN_DEVI void unit_coords(int u, const GemmArgs& a, int& mb, int& nb, int& half
     half = h & 1;
   }
 }
+// The raster: the N-blocks are cut into bands of band_n blocks; within a band,
+// groups of GROUP_M pair M-blocks sweep the band's N-blocks with the M-block
+// varying fastest (concurrent tiles share weight slices in L2), and odd groups
+// sweep backwards (serpentine), so a group starts on the weight slices the
+// previous group read last.  A band small enough to stay in L2 is read once
+// while the activation groups cycle through it.
 QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
-  const int per_group = GROUP_M * a.tiles_n;
-  const int group = tile / per_group;
+  const int band_tiles = a.tiles_m * a.band_n;
+  const int band = tile / band_tiles;
+  const int n0 = band * a.band_n;
+  const int wb = min(a.band_n, a.tiles_n - n0);          // N-blocks of this band (the last may be short)
+  const int t = tile - band * band_tiles;
+  const int per_group = GROUP_M * wb;
+  const int group = t / per_group;
   const int first_m = group * GROUP_M;
   const int gsize = min(a.tiles_m - first_m, GROUP_M);
-  const int r = tile - group * per_group;
+  const int r = t - group * per_group;
   mb = first_m + r % gsize;
-  // serpentine: odd groups sweep the N-blocks backwards, so a group starts on
-  // the weight slices the previous group read last (still in L2).  Measured at
-  // the 8B shape (ncu DRAM bytes per launch): gate|up reads 1006 -> 816 MB,
-  // down 1019 -> 920 MB, same time.
-  nb = (group & 1) ? a.tiles_n - 1 - r / gsize : r / gsize;
+  nb = n0 + ((group & 1) ? wb - 1 - r / gsize : r / gsize);
 }
 
 template <int EPI, bool A_MN = false, bool B_MN = false>
@@ -966,6 +974,10 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
   a.tiles_m = int((M + 2 * BM - 1) / (2 * BM));
   a.tiles_n = int((N + BN - 1) / BN);
   a.num_tiles = a.tiles_m * a.tiles_n;
+  // one band: the bf16-output GEMMs' activation operand is the larger one
+  // (down: 235 MB against 59 MB of weights), and cutting the weights into
+  // bands re-reads it per band (measured: 1.1-1.45 GB read instead of 0.92)
+  a.band_n = a.tiles_n;
   a.num_kb = int((K + KBOX * BK - 1) / (KBOX * BK));
   a.split_from = a.num_tiles;
   // the output tensor map of the epilogue's TMA stores (and, when
@@ -986,6 +998,17 @@ cudaError_t launch_gemm_bf16(uint16_t* out, const uint8_t* A, const float* a_sca
 }
 
 namespace {
+// N-blocks per raster band of the SwiGLU forms: about 32 MB of W1 (an N-block
+// is 128 gate and 128 up rows of K bytes).  Measured at the 8B shape (ncu DRAM
+// bytes per launch of the gate|up GEMM): one band 817 MB read, bands of 16 MB
+// 595, 32 MB 544, 64 MB 694; time within 2%.
+int band_blocks(int tiles_n, int64_t K) {
+  const int64_t per = int64_t(256) * K;
+  int64_t b = (int64_t(32) << 20) / (per > 0 ? per : 1);
+  if (b < 1) b = 1;
+  return b > tiles_n ? tiles_n : int(b);
+}
+
 // Tensor maps and arguments shared by the two SwiGLU forms.
 bool swiglu_args(GemmArgs* a, CUtensorMap* ma, CUtensorMap* mb, void* out, float* stats_h,
                  const uint8_t* A, const float* a_scale, const uint8_t* W1, const float* w_scale,
@@ -1003,6 +1026,7 @@ bool swiglu_args(GemmArgs* a, CUtensorMap* ma, CUtensorMap* mb, void* out, float
   a->tiles_m = int((M + 2 * BM - 1) / (2 * BM));
   a->tiles_n = int(H / 128);
   a->num_tiles = a->tiles_m * a->tiles_n;
+  a->band_n = band_blocks(a->tiles_n, K);
   a->num_kb = int((K + KBOX * BK - 1) / (KBOX * BK));
   a->split_from = a->num_tiles;
   return true;
