@@ -900,6 +900,18 @@ def profile_case(q, torch, device):
     print("profile case done")
 
 
+def profile_workload(q, torch, device, cfg):
+    """The prefill chain of one of the pages' workloads three times, untimed (for ncu
+    captures of the small workloads; launch order per forward: rmsnorm, quantize, gate|up
+    GEMM, quantize, down GEMM)."""
+    d = prefill_setup(q, torch, device, cfg)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(3):
+        forward(q, d, stream, cfg)
+    torch.cuda.synchronize()
+    q.qffn_check_status(stream)
+
+
 def traffic_case(q, torch, device):
     """A case for one ncu capture of DRAM bytes per launch (about 1.2 GB on the device):
     the gate|up GEMM with the SwiGLU epilogue and the down GEMM at the 8B prefill shape
@@ -949,6 +961,8 @@ def main():
     ap.add_argument("--decode-iters", type=int, default=300)
     ap.add_argument("--profile-case", action="store_true",
                     help="run a small case once (for ncu captures) and exit without timing")
+    ap.add_argument("--profile-workload", choices=sorted(PREFILL),
+                    help="run the prefill chain of one workload three times (for ncu captures) and exit")
     ap.add_argument("--traffic-case", action="store_true",
                     help="run the full-size GEMMs and decode twice (for an ncu DRAM-bytes capture) and exit")
     args = ap.parse_args()
@@ -968,6 +982,9 @@ def main():
         return
     if args.traffic_case:
         traffic_case(q, torch, device)
+        return
+    if args.profile_workload:
+        profile_workload(q, torch, device, PREFILL[args.profile_workload])
         return
     peaks = load_peaks()
     pre = bench_prefill(q, torch, device, args.steps, args.warmup, dist, peaks)

@@ -202,7 +202,10 @@ def test_fp8_gemm_identity_weight(q):
 @pytest.mark.parametrize("N,C,H", [(64, 256, 768), (1, 128, 128), (200, 384, 256), (513, 2048, 1024),
                                    # 80 tiles: the last wave runs as half tiles (64 gate +
                                    # 64 up columns), the second with a ragged last M-block
-                                   (5120, 64, 512), (4900, 96, 512)])
+                                   (5120, 64, 512), (4900, 96, 512),
+                                   # K > 2048: the eight-column epilogue step (the shapes
+                                   # above take the sixteen-column one), whole and half tiles
+                                   (130, 2176, 384), (5120, 2304, 512)])
 def test_gate_up_swiglu(q, N, C, H):
     """The fused epilogue equals SwiGLU applied to the GPU's own unfused gate|up GEMM
     (same accumulators, same bf16 rounding of g and u), within 1 ulp of the fp64 silu."""

@@ -29,7 +29,9 @@ def _gate_up_inputs(N, C, H, seed):
 @pytest.mark.parametrize("N,C,H", [(64, 256, 768), (1, 128, 128), (200, 384, 256), (513, 2048, 1024),
                                    (300, 4096, 14336),
                                    # the last wave as half tiles, one with a ragged last M-block
-                                   (5120, 64, 512), (4900, 96, 512)])
+                                   (5120, 64, 512), (4900, 96, 512),
+                                   # K > 2048 (the eight-column epilogue step), half tiles
+                                   (5120, 2304, 512)])
 def test_gate_up_swiglu_quant_equals_two_pass(q, N, C, H):
     """E4M3 straight from the epilogue == quantize of the bf16 h the SwiGLU epilogue
     writes, with the abs-max that call recorded (codes and scale bit for bit)."""

@@ -299,6 +299,58 @@ QFFN_DEVI void tmem_ld8x2(uint32_t ta, uint32_t tb, uint32_t (&a)[8], uint32_t (
       : "memory");
 }
 
+// Issue the loads of sixteen 32-bit TMEM columns at each of two addresses
+// (this warp's lane quarter) without waiting; tmem_wait_ld16 makes them usable.
+QFFN_DEVI void tmem_ld16x2_issue(uint32_t ta, uint32_t tb, uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+// Wait for this thread's TMEM loads.  The registers of the load being waited
+// for pass through the wait, so that no use of them is placed before it.
+QFFN_DEVI void tmem_wait_ld16(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]), "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]), "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
+               :
+               : "memory");
+}
+// Running max of |v| over bf16 pairs: lane-wise max of m and the absolute
+// values of the two bf16 in v (exact, no rounding).
+QFFN_DEVI uint32_t bf16x2_absmax(uint32_t m, uint32_t v) {
+  uint32_t a, r;
+  asm("abs.bf16x2 %0, %1;" : "=r"(a) : "r"(v));
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(a));
+  return r;
+}
+
+// h for two adjacent accumulator columns: the packed bf16 pair
+// (silu(g0) * u0, silu(g1) * u1) with g, u the scaled accumulators rounded to
+// bf16 -- silu_mul_f32 on each, the multiplications done pairwise by f32x2
+// instructions (each lane rounds as the scalar instruction does, so the
+// result is the same bits).
+QFFN_DEVI uint32_t swiglu_pair(uint32_t ga, uint32_t gb, uint32_t ua, uint32_t ub, uint64_t scale2) {
+  float g0, g1, u0, u1;
+  f2_unpack(f2_mul(f2_pack(__uint_as_float(ga), __uint_as_float(gb)), scale2), g0, g1);
+  f2_unpack(f2_mul(f2_pack(__uint_as_float(ua), __uint_as_float(ub)), scale2), u0, u1);
+  const uint32_t gr = pack_bf16x2(g0, g1), ur = pack_bf16x2(u0, u1);
+  const uint64_t G = f2_pack(bf16_lo(gr), bf16_hi(gr));
+  const uint64_t U = f2_pack(bf16_lo(ur), bf16_hi(ur));
+  const float e0 = __expf(-fabsf(bf16_lo(gr))), e1 = __expf(-fabsf(bf16_hi(gr)));
+  const uint64_t E = f2_pack(e0, e1);
+  float d0, d1;
+  f2_unpack(f2_add(f2_pack(1.0f, 1.0f), E), d0, d1);
+  const float r0 = __fdividef(1.0f, d0), r1 = __fdividef(1.0f, d1);
+  float er0, er1;
+  f2_unpack(f2_mul(E, f2_pack(r0, r1)), er0, er1);
+  const uint64_t S = f2_pack(bf16_lo(gr) >= 0.0f ? r0 : er0, bf16_hi(gr) >= 0.0f ? r1 : er1);
+  float h0, h1;
+  f2_unpack(f2_mul(f2_mul(G, S), U), h0, h1);
+  return pack_bf16x2(h0, h1);
+}
+
 // Pair tile -> (pair M-block of 256 rows, N-block)
 QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb);
 // Work unit -> (pair M-block, N-block, half): half = -1 for a whole tile,
@@ -334,7 +386,7 @@ QFFN_DEVI void tile_coords(int tile, const GemmArgs& a, int& mb, int& nb) {
   nb = n0 + ((group & 1) ? wb - 1 - r / gsize : r / gsize);
 }
 
-template <int EPI, bool A_MN = false, bool B_MN = false>
+template <int EPI, bool A_MN = false, bool B_MN = false, bool WIDE = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmC,
@@ -505,6 +557,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row_in_tile = int(rank) * BM + q * 32 + lane;
     const float scale = args.a_scale[0] * args.w_scale[0];
     float amax = 0.0f;
+    uint32_t amax2 = 0u;     // WIDE EPI_SWIGLU: running max of |h| on bf16 pairs (exact)
+    const uint64_t scale2 = f2_pack(scale, scale);
     int sbuf = 0;            // TMA-store forms: which of this warp's two staging boxes is next
     // EPI_SWIGLU_E4M3: quantise h with the given abs-max, as quantize_with_abs_max
     // does (fp32 product with 448 / abs_max, nearest even, saturating)
@@ -730,65 +784,140 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int up_off = half < 0 ? 128 : 64;               // accumulator column of u
         const size_t hoff = size_t(row) * size_t(args.N) + size_t(nb) * 128 + size_t(hbase);
         uint8_t* qrow = static_cast<uint8_t*>(args.out) + hoff;
-        // Eight columns of g and u per step in a rolled loop: the epilogue's
-        // code stays small, so it does not crowd the producer's and the MMA
-        // issuer's loops out of the instruction cache of the SM sub-partitions
-        // it shares with them (measured: 2.4% fewer cycles per GEMM than a
-        // fully unrolled 32-column step).
-#pragma unroll 1
-        for (int c0 = 0; c0 < hcols; c0 += 8) {
-          uint32_t g[8], u[8];
-          tmem_ld8x2(tbase + uint32_t(c0), tbase + uint32_t(up_off + c0), g, u);
-          {
-            // EPI_SWIGLU stages h in shared memory and stores it with TMA, one
-            // 32-row x 64-column box per warp and half tile: each lane writes
-            // its row's 16 bytes into the 128-byte-swizzled box (4 wavefronts
-            // per warp store), where per-thread 16-byte global stores would
-            // touch 32 rows per instruction.
-            uint8_t* sbox = sStaging + (q * 2 + sbuf) * STAGE_BOX_BYTES;
-            if (EPI == EPI_SWIGLU && (c0 & 63) == 0) {
-              if (lane == 0) bulk_wait_read_1();   // the store that last read this box is done
-              __syncwarp();
-            }
-            uint32_t p[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float g0 = round_bf16(__uint_as_float(g[2 * j]) * scale);
-              const float g1 = round_bf16(__uint_as_float(g[2 * j + 1]) * scale);
-              const float u0 = round_bf16(__uint_as_float(u[2 * j]) * scale);
-              const float u1 = round_bf16(__uint_as_float(u[2 * j + 1]) * scale);
-              p[j] = pack_bf16x2(silu_mul_f32(g0, u0), silu_mul_f32(g1, u1));
-              if (EPI == EPI_SWIGLU && row_ok)
-                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
-            }
-            if (EPI == EPI_SWIGLU) {
-              const int chunk = (c0 & 63) >> 3;
-              *reinterpret_cast<uint4*>(sbox + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
-                  make_uint4(p[0], p[1], p[2], p[3]);
-              if (chunk == 7) {
-                fence_proxy_async_smem();
+        if constexpr (WIDE) {
+          // Sixteen columns of g and u per step, two steps per turn of a rolled
+          // loop: the epilogue's code stays small, so it does not crowd the
+          // producer's and the MMA issuer's loops out of the instruction cache
+          // of the SM sub-partitions it shares with them (measured: 2.4% fewer
+          // cycles per GEMM than a fully unrolled 32-column step).  One warp per
+          // sub-partition runs this loop, so its rate is set by the
+          // instruction-level parallelism of a step: sixteen columns give
+          // sixteen independent SwiGLU chains, their multiplications paired in
+          // f32x2 instructions.  The TMEM load of the next step is issued
+          // before this step's arithmetic.
+          uint32_t gq[2][16], uq[2][16];
+          tmem_ld16x2_issue(tbase, tbase + uint32_t(up_off), gq[0], uq[0]);
+  #pragma unroll 1
+          for (int c00 = 0; c00 < hcols; c00 += 32) {
+  #pragma unroll
+            for (int st = 0; st < 2; ++st) {
+              const int c0 = c00 + 16 * st;
+              tmem_wait_ld16(gq[st], uq[st]);          // this step's columns have landed
+              if (c0 + 16 < hcols) {
                 __syncwarp();
-                const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
-                if (lane == 0) {
-                  if (row0 < args.M)
-                    tma_store_2d(&tmC, smem_u32(sbox), nb * 128 + hbase + (c0 & ~63), row0);
-                  bulk_commit();
+                tmem_ld16x2_issue(tbase + uint32_t(c0 + 16), tbase + uint32_t(up_off + c0 + 16),
+                                  gq[st ^ 1], uq[st ^ 1]);
+              }
+              // EPI_SWIGLU stages h in shared memory and stores it with TMA, one
+              // 32-row x 64-column box per warp and half tile: each lane writes
+              // its row's 16-byte chunks into the 128-byte-swizzled box (4
+              // wavefronts per warp store), where per-thread 16-byte global
+              // stores would touch 32 rows per instruction.
+              uint8_t* sbox = sStaging + (q * 2 + sbuf) * STAGE_BOX_BYTES;
+              if (EPI == EPI_SWIGLU && (c0 & 63) == 0) {
+                if (lane == 0) bulk_wait_read_1();   // the store that last read this box is done
+                __syncwarp();
+              }
+              uint32_t p[8];
+  #pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                p[j] = swiglu_pair(gq[st][2 * j], gq[st][2 * j + 1], uq[st][2 * j], uq[st][2 * j + 1], scale2);
+                if (EPI == EPI_SWIGLU && row_ok) amax2 = bf16x2_absmax(amax2, p[j]);
+              }
+              if (EPI == EPI_SWIGLU) {
+                const int chunk = (c0 & 63) >> 3;      // even: this step fills chunks chunk, chunk + 1
+  #pragma unroll
+                for (int k = 0; k < 2; ++k)
+                  *reinterpret_cast<uint4*>(sbox + lane * 128 + (((chunk + k) ^ (lane & 7)) << 4)) =
+                      make_uint4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]);
+                if (chunk == 6) {
+                  fence_proxy_async_smem();
+                  __syncwarp();
+                  const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
+                  if (lane == 0) {
+                    if (row0 < args.M)
+                      tma_store_2d(&tmC, smem_u32(sbox), nb * 128 + hbase + (c0 & ~63), row0);
+                    bulk_commit();
+                  }
+                  sbuf ^= 1;
                 }
-                sbuf ^= 1;
+              }
+              if (EPI == EPI_SWIGLU_E4M3 && row_ok) {
+                uint32_t c[4];
+  #pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const uint16_t lo = qzero ? uint16_t(0)
+                                            : f32x2_to_e4m3x2(bf16_lo(p[2 * j]) * qinv, bf16_hi(p[2 * j]) * qinv);
+                  const uint16_t hi = qzero ? uint16_t(0)
+                                            : f32x2_to_e4m3x2(bf16_lo(p[2 * j + 1]) * qinv,
+                                                              bf16_hi(p[2 * j + 1]) * qinv);
+                  c[j] = uint32_t(lo) | (uint32_t(hi) << 16);
+                }
+                *reinterpret_cast<uint4*>(qrow + c0) = make_uint4(c[0], c[1], c[2], c[3]);
               }
             }
-            if (EPI == EPI_SWIGLU_E4M3 && row_ok) {
-              uint32_t c[2];
-#pragma unroll
-              for (int j = 0; j < 2; ++j) {
-                const uint16_t lo = qzero ? uint16_t(0)
-                                          : f32x2_to_e4m3x2(bf16_lo(p[2 * j]) * qinv, bf16_hi(p[2 * j]) * qinv);
-                const uint16_t hi = qzero ? uint16_t(0)
-                                          : f32x2_to_e4m3x2(bf16_lo(p[2 * j + 1]) * qinv,
-                                                            bf16_hi(p[2 * j + 1]) * qinv);
-                c[j] = uint32_t(lo) | (uint32_t(hi) << 16);
+          }
+        } else {
+          // Eight columns of g and u per step in a rolled loop: the epilogue's
+          // code stays small, so it does not crowd the producer's and the MMA
+          // issuer's loops out of the instruction cache of the SM sub-partitions
+          // it shares with them (measured: 2.4% fewer cycles per GEMM than a
+          // fully unrolled 32-column step).
+  #pragma unroll 1
+          for (int c0 = 0; c0 < hcols; c0 += 8) {
+            uint32_t g[8], u[8];
+            tmem_ld8x2(tbase + uint32_t(c0), tbase + uint32_t(up_off + c0), g, u);
+            {
+              // EPI_SWIGLU stages h in shared memory and stores it with TMA, one
+              // 32-row x 64-column box per warp and half tile: each lane writes
+              // its row's 16 bytes into the 128-byte-swizzled box (4 wavefronts
+              // per warp store), where per-thread 16-byte global stores would
+              // touch 32 rows per instruction.
+              uint8_t* sbox = sStaging + (q * 2 + sbuf) * STAGE_BOX_BYTES;
+              if (EPI == EPI_SWIGLU && (c0 & 63) == 0) {
+                if (lane == 0) bulk_wait_read_1();   // the store that last read this box is done
+                __syncwarp();
               }
-              *reinterpret_cast<uint2*>(qrow + c0) = make_uint2(c[0], c[1]);
+              uint32_t p[4];
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float g0 = round_bf16(__uint_as_float(g[2 * j]) * scale);
+                const float g1 = round_bf16(__uint_as_float(g[2 * j + 1]) * scale);
+                const float u0 = round_bf16(__uint_as_float(u[2 * j]) * scale);
+                const float u1 = round_bf16(__uint_as_float(u[2 * j + 1]) * scale);
+                p[j] = pack_bf16x2(silu_mul_f32(g0, u0), silu_mul_f32(g1, u1));
+                if (EPI == EPI_SWIGLU && row_ok)
+                  amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(p[j])), fabsf(bf16_hi(p[j]))));
+              }
+              if (EPI == EPI_SWIGLU) {
+                const int chunk = (c0 & 63) >> 3;
+                *reinterpret_cast<uint4*>(sbox + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
+                    make_uint4(p[0], p[1], p[2], p[3]);
+                if (chunk == 7) {
+                  fence_proxy_async_smem();
+                  __syncwarp();
+                  const int row0 = mb * (2 * BM) + int(rank) * BM + q * 32;
+                  if (lane == 0) {
+                    if (row0 < args.M)
+                      tma_store_2d(&tmC, smem_u32(sbox), nb * 128 + hbase + (c0 & ~63), row0);
+                    bulk_commit();
+                  }
+                  sbuf ^= 1;
+                }
+              }
+              if (EPI == EPI_SWIGLU_E4M3 && row_ok) {
+                uint32_t c[2];
+  #pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  const uint16_t lo = qzero ? uint16_t(0)
+                                            : f32x2_to_e4m3x2(bf16_lo(p[2 * j]) * qinv, bf16_hi(p[2 * j]) * qinv);
+                  const uint16_t hi = qzero ? uint16_t(0)
+                                            : f32x2_to_e4m3x2(bf16_lo(p[2 * j + 1]) * qinv,
+                                                              bf16_hi(p[2 * j + 1]) * qinv);
+                  c[j] = uint32_t(lo) | (uint32_t(hi) << 16);
+                }
+                *reinterpret_cast<uint2*>(qrow + c0) = make_uint2(c[0], c[1]);
+              }
             }
           }
         }
@@ -806,6 +935,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (EPI == EPI_SWIGLU_BWD && lane == 0 && dh_pending)
       mbar_wait(dh_bar(q), dh_par, abort_flag, false, kDrainLimitNs);
     if (EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD) {
+      if (EPI == EPI_SWIGLU && WIDE) amax = fmaxf(amax, fmaxf(bf16_lo(amax2), bf16_hi(amax2)));
       amax = warp_max(amax);
       if (lane == 0) atomic_max_nonneg(args.amax, amax);
     }
@@ -870,7 +1000,7 @@ bool make_store_map_bf16(CUtensorMap* map, uint16_t* ptr, int64_t rows, int64_t 
 
 // Number of 2-CTA clusters of this kernel that fit on the device at once
 // (cached per device and form).
-template <int EPI, bool A_MN = false, bool B_MN = false>
+template <int EPI, bool A_MN = false, bool B_MN = false, bool WIDE = false>
 cudaError_t max_pairs(int* pairs) {
   static int cached[64] = {0};
   int dev = 0;
@@ -880,7 +1010,7 @@ cudaError_t max_pairs(int* pairs) {
     *pairs = cached[dev];
     return cudaSuccess;
   }
-  e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI, A_MN, B_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI, A_MN, B_MN, WIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -895,7 +1025,7 @@ cudaError_t max_pairs(int* pairs) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  e = cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI, A_MN, B_MN>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&n, gemm_fp8_kernel<EPI, A_MN, B_MN, WIDE>, &cfg);
   if (e != cudaSuccess) return e;
   if (n < 1) return cudaErrorInvalidConfiguration;
   if (dev >= 0 && dev < 64) cached[dev] = n;
@@ -903,12 +1033,12 @@ cudaError_t max_pairs(int* pairs) {
   return cudaSuccess;
 }
 
-template <int EPI, bool A_MN = false, bool B_MN = false>
+template <int EPI, bool A_MN = false, bool B_MN = false, bool WIDE = false>
 cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cudaStream_t s,
                    const CUtensorMap* mc = nullptr, bool pdl = false,
                    const CUtensorMap* md = nullptr) {
   int pairs = 0;
-  cudaError_t e = max_pairs<EPI, A_MN, B_MN>(&pairs);
+  cudaError_t e = max_pairs<EPI, A_MN, B_MN, WIDE>(&pairs);
   if (e != cudaSuccess) return e;
   if (a.num_tiles < pairs) pairs = a.num_tiles;
   cudaLaunchConfig_t cfg = {};
@@ -925,7 +1055,7 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, A_MN, B_MN>, ma, mb, mc != nullptr ? *mc : ma,
+  return cudaLaunchKernelEx(&cfg, gemm_fp8_kernel<EPI, A_MN, B_MN, WIDE>, ma, mb, mc != nullptr ? *mc : ma,
                             md != nullptr ? *md : ma, a);
 }
 
@@ -933,11 +1063,11 @@ cudaError_t launch(const CUtensorMap& ma, const CUtensorMap& mb, GemmArgs a, cud
 // in half a tile's time: sets split_from and num_tiles, and the weight tensor
 // map with 64-row boxes that the half tiles' B loads use.  Leaves the
 // arguments unchanged otherwise.
-template <int EPI>
+template <int EPI, bool WIDE = false>
 cudaError_t split_last_wave(GemmArgs* a, CUtensorMap* mb_half, const uint8_t* W, int64_t wrows,
                             int64_t K) {
   int pairs = 0;
-  cudaError_t e = max_pairs<EPI>(&pairs);
+  cudaError_t e = max_pairs<EPI, false, false, WIDE>(&pairs);
   if (e != cudaSuccess) return e;
   const int r = a->num_tiles % pairs;
   if (a->num_tiles > pairs && r > 0 && 2 * r <= pairs) {
@@ -1009,6 +1139,15 @@ int band_blocks(int tiles_n, int64_t K) {
   return b > tiles_n ? tiles_n : int(b);
 }
 
+// The SwiGLU forward forms' epilogue: sixteen columns per step (WIDE) when a
+// tile's main loop is at most 8 stages (K <= 2048), where the epilogue and
+// not the MMAs sets the tile rate; eight otherwise.  Per-tile clock stamps at
+// K = 2048 (Llama-3.2-1B gate|up): main loop 4.07 us, epilogue 5.0 us with
+// eight columns per step.  Measured, gate|up alone, interleaved: K = 2048
+// 0.091 -> 0.082 ms with the wide step; K = 3584 and 4096 0.541 -> 0.558 and
+// 0.924 -> 0.948 ms, so the long-K forms keep the narrow step.
+bool wide_epilogue(int64_t K) { return K <= 2048; }
+
 // Tensor maps and arguments shared by the two SwiGLU forms.
 bool swiglu_args(GemmArgs* a, CUtensorMap* ma, CUtensorMap* mb, void* out, float* stats_h,
                  const uint8_t* A, const float* a_scale, const uint8_t* W1, const float* w_scale,
@@ -1048,6 +1187,12 @@ cudaError_t launch_gemm_swiglu(uint16_t* h, float* stats_h, const uint8_t* A, co
   CUtensorMap mc;
   if (!make_store_map_bf16(&mc, h, M, H)) return cudaErrorInvalidValue;
   CUtensorMap mb_half;
+  if (wide_epilogue(K)) {
+    cudaError_t e = split_last_wave<EPI_SWIGLU, true>(&a, &mb_half, W1, 2 * H, K);
+    if (e != cudaSuccess) return e;
+    return launch<EPI_SWIGLU, false, false, true>(ma, mb, a, s, &mc, chained,
+                                                  a.split_from < a.num_tiles ? &mb_half : nullptr);
+  }
   cudaError_t e = split_last_wave<EPI_SWIGLU>(&a, &mb_half, W1, 2 * H, K);
   if (e != cudaSuccess) return e;
   return launch<EPI_SWIGLU>(ma, mb, a, s, &mc, chained,
@@ -1065,6 +1210,12 @@ cudaError_t launch_gemm_swiglu_quant(uint8_t* hq, float* stats_h, const uint8_t*
   if (!swiglu_args(&a, &ma, &mb, hq, stats_h, A, a_scale, W1, w_scale, M, H, K))
     return cudaErrorInvalidValue;
   CUtensorMap mb_half;
+  if (wide_epilogue(K)) {
+    cudaError_t e = split_last_wave<EPI_SWIGLU_E4M3, true>(&a, &mb_half, W1, 2 * H, K);
+    if (e != cudaSuccess) return e;
+    return launch<EPI_SWIGLU_E4M3, false, false, true>(ma, mb, a, s, nullptr, pdl,
+                                                       a.split_from < a.num_tiles ? &mb_half : nullptr);
+  }
   cudaError_t e = split_last_wave<EPI_SWIGLU_E4M3>(&a, &mb_half, W1, 2 * H, K);
   if (e != cudaSuccess) return e;
   return launch<EPI_SWIGLU_E4M3>(ma, mb, a, s, nullptr, pdl,
