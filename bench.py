@@ -42,7 +42,7 @@ FP8_PER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor rate ratio
 # capture of this benchmark's full-size workload (dram__bytes_read.sum +
 # dram__bytes_write.sum).  Set to None whenever the kernel changes until it
 # is captured again.
-TRAFFIC_GATE_UP_BYTES = (551.0 + 443.8) * 1e6
+TRAFFIC_GATE_UP_BYTES = (551.8 + 443.8) * 1e6
 TRAFFIC_DUAL_GEMV_BYTES = (117.6 + 0.1) * 1e6
 
 
@@ -216,6 +216,28 @@ def staged_forward(q, d, stream, ev, cfg=None):
     ev[5].record(stream)
 
 
+def gemm_clock_mhz(q, d, stream, steps):
+    """Mean SM clock (MHz) of the gate|up and of the down GEMM at the end of `steps`
+    back-to-back forwards (the power state of the timed region), from each GEMM's own
+    clock sample: %clock64 cycles over %globaltimer ns of its first CTA."""
+    cfg = PREFILL_CFG
+    N, C, H = cfg.N, cfg.C, cfg.H
+    st = d["stats"]
+    for _ in range(steps):
+        forward(q, d, stream)
+    cyc, ns = q.qffn_gemm_clock_sample(stream)        # the last down GEMM
+    down = cyc / ns * 1e3
+    for _ in range(steps - 1):
+        forward(q, d, stream)
+    q.qffn_rmsnorm_absmax(d["res_out"], d["y"], d["rstd"], st[0:2], d["res"], d["x"], d["gain"],
+                          cfg.eps, N, C, stream=stream)
+    q.qffn_quantize(d["yq"], st[0:2], d["y"], N * C, stream=stream)
+    q.qffn_gate_up_swiglu(d["h"], st[2:4], d["yq"], st[1:2], d["w1"], d["w1_scale"], N, C, H,
+                          stream=stream)
+    cyc, ns = q.qffn_gemm_clock_sample(stream)
+    return cyc / ns * 1e3, down
+
+
 def bench_prefill(q, torch, device, steps, warmup, dist, peaks):
     cfg = PREFILL_CFG
     N, C, H = cfg.N, cfg.C, cfg.H
@@ -250,6 +272,8 @@ def bench_prefill(q, torch, device, steps, warmup, dist, peaks):
     q.qffn_check_status(stream)
     stage_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in evs) for j in range(5)]
     staged_total = statistics.mean(e[0].elapsed_time(e[5]) for e in evs)
+    gu_mhz, down_mhz = gemm_clock_mhz(q, d, stream, steps)
+    q.qffn_check_status(stream)
     ms_total = max_over_ranks(dist, ms_total)
     ms_step = ms_total / steps
 
@@ -326,6 +350,16 @@ def bench_prefill(q, torch, device, steps, warmup, dist, peaks):
                      "peak_note": f"{peaks['source']} bf16 burst x {FP8_PER_BF16:g} (nominal FP8/BF16 ratio)"},
         "clocks": clk.summary(),
         "launches_per_step": 5,
+    }
+    # the tensor cores' rate per clock at the clock the GEMMs themselves ran at
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    per_clock_peak = sms * gu_mhz * 1e6 * FP8_FLOP_PER_CLK_PER_SM / 1e12
+    res["gemm_clock"] = {
+        "gate_up_sm_mhz": gu_mhz, "down_sm_mhz": down_mhz,
+        "source": "each GEMM's first CTA: %clock64 cycles / %globaltimer ns from its start to its end "
+                  "(qffn_gemm_clock_sample), after back-to-back forwards",
+        "gate_up_per_clock_peak_tflops": per_clock_peak,
+        "gate_up_frac_of_per_clock_peak": achieved / per_clock_peak,
     }
     # HBM-side fractions of the elementwise stages (algorithmic bytes / time)
     hbm = peaks["hbm_gbs"]
@@ -1008,6 +1042,7 @@ def main():
                    "l2": "inputs larger than L2 (per-step working set ~3 GB)"},
         "roofline": pre["roofline"],
         "clocks": pre["clocks"],
+        "gemm_clock": pre["gemm_clock"],
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": pre["e2e_bytes"][0],
                 "d2h_bytes_per_step": pre["e2e_bytes"][1]},
         "gpu_launches": pre["launches_per_step"] * args.steps,

@@ -73,6 +73,17 @@ int qffn_abi_version(void);
  * check, QFFN_ERR_CUDA if the synchronisation failed, else QFFN_OK. */
 qffn_status qffn_check_status(qffn_stream_t stream);
 
+/* Measurement aid (no counterpart on the pages).  Synchronises `stream`, then
+ * writes, for the most recent GEMM launch on the current device, the SM clock
+ * cycles (%clock64) and the nanoseconds (%globaltimer) that its first CTA
+ * spent from its start to its end: out[0] / out[1] is the mean SM clock of
+ * that launch in GHz.  With the tensor cores' dense FP8 rate of 16384 FLOP
+ * per clock per SM it gives the peak the launch could reach at the clock it
+ * ran at.  Both are 0 before the first GEMM launch of the process.
+ *   out: host, 2 x uint64.  QFFN_ERR_CUDA if the synchronisation or the read
+ *   fails. */
+qffn_status qffn_gemm_clock_sample(uint64_t* out, qffn_stream_t stream);
+
 /* Self-test of the failure path (no counterpart on the pages, which stop on
  * any CUDA error; this library bounds its device-side waits instead).  One
  * CTA runs the GEMMs' bounded barrier wait on two barriers of arrival count 1:

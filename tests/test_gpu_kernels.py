@@ -198,6 +198,25 @@ def test_fp8_gemm_identity_weight(q):
     np.testing.assert_array_equal(oracle.bf16_to_f64(bf(out)), oracle.bf16_to_f64(want))
 
 
+def test_gemm_clock_sample(q):
+    """The clock sample of a GEMM launch: positive SM cycles and nanoseconds whose ratio
+    (the mean SM clock of the launch) lies in the part's range, and a later launch
+    replaces the sample."""
+    M = N = K = 2048
+    a = random_codes((M, K), seed=91)
+    w = random_codes((N, K), seed=92)
+    scales = torch.tensor([0.5, 0.25], dtype=torch.float32, device="cuda")
+    out = empty_bf16(M, N)
+    q.qffn_fp8_gemm_scaled(out, dev(a), scales[0:1], dev(w), scales[1:2], M, N, K)
+    cyc, ns = q.qffn_gemm_clock_sample()
+    assert cyc > 0 and ns > 0
+    assert 0.3 < cyc / ns < 2.5, (cyc, ns)
+    out2 = empty_bf16(4 * M, N)
+    q.qffn_fp8_gemm_scaled(out2, dev(np.concatenate([a] * 4)), scales[0:1], dev(w), scales[1:2], 4 * M, N, K)
+    cyc2, ns2 = q.qffn_gemm_clock_sample()
+    assert (cyc2, ns2) != (cyc, ns) and 0.3 < cyc2 / ns2 < 2.5, (cyc2, ns2)
+
+
 # ------------------------------------------------------------------ A3+A4 fused
 @pytest.mark.parametrize("N,C,H", [(64, 256, 768), (1, 128, 128), (200, 384, 256), (513, 2048, 1024),
                                    # 80 tiles: the last wave runs as half tiles (64 gate +

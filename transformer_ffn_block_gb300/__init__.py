@@ -18,6 +18,7 @@ from ._build import build
 __all__ = [
     "QffnError", "lib", "build", "LIB_PATH", "STATUS",
     "qffn_status_string", "qffn_abi_version", "qffn_check_status", "qffn_selftest_bounded_wait",
+    "qffn_gemm_clock_sample",
     "qffn_rmsnorm_absmax", "qffn_absmax", "qffn_quantize", "qffn_quantize_rows",
     "qffn_fp8_gemm_scaled", "qffn_qmm", "qffn_gate_up_swiglu", "qffn_swiglu_quant",
     "qffn_swiglu_forward_quant", "qffn_gate_up_swiglu_quant",
@@ -53,6 +54,7 @@ _SIGS = {
     "qffn_abi_version": ([], ctypes.c_int),
     "qffn_check_status": ([_P], _S),
     "qffn_selftest_bounded_wait": ([_P, _S, _I64, _P], _S),
+    "qffn_gemm_clock_sample": ([_P, _P], _S),
     "qffn_rmsnorm_absmax": ([_P, _P, _P, _P, _P, _P, _P, _F, _I64, _I64, _P], _S),
     "qffn_absmax": ([_P, _P, _I64, _P], _S),
     "qffn_quantize": ([_P, _P, _P, _I64, _P], _S),
@@ -139,6 +141,14 @@ def qffn_check_status(stream=None):
 def qffn_selftest_bounded_wait(out, arrive, limit_ns, stream=None):
     _check("qffn_selftest_bounded_wait", lib.qffn_selftest_bounded_wait(
         _ptr(out), int(bool(arrive)), int(limit_ns), _stream(stream)))
+
+
+def qffn_gemm_clock_sample(stream=None):
+    """(SM clock cycles, nanoseconds) of the first CTA of the most recent GEMM launch."""
+    out = (ctypes.c_uint64 * 2)()
+    _check("qffn_gemm_clock_sample", lib.qffn_gemm_clock_sample(
+        ctypes.cast(out, ctypes.c_void_p), _stream(stream)))
+    return int(out[0]), int(out[1])
 
 
 def qffn_rmsnorm_absmax(res_out, y, rstd, stats, res_in, x, gain, eps, N, C, stream=None):

@@ -152,6 +152,16 @@ qffn_status qffn_check_status(qffn_stream_t stream) {
   return (st | sd) != 0 ? QFFN_ERR_TIMEOUT : QFFN_OK;
 }
 
+qffn_status qffn_gemm_clock_sample(uint64_t* out, qffn_stream_t stream) {
+  QFFN_PTR(out);
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return QFFN_ERR_CUDA;
+  unsigned long long v[2] = {0ull, 0ull};
+  if (qffn::gemm_clock_sample(v) != cudaSuccess) return QFFN_ERR_CUDA;
+  out[0] = v[0];
+  out[1] = v[1];
+  return QFFN_OK;
+}
+
 qffn_status qffn_selftest_bounded_wait(uint64_t* out, int arrive, int64_t limit_ns,
                                        qffn_stream_t stream) {
   QFFN_RANGE();

@@ -115,6 +115,9 @@ constexpr uint32_t kStepK = UMMA_K;
 constexpr uint32_t kStepMN = UMMA_K * 128;
 
 __device__ unsigned int g_status;
+// SM clock cycles and nanoseconds from start to end of the first CTA of the
+// most recent launch (read by gemm_clock_sample).
+__device__ unsigned long long g_clock_sample[2];
 
 // Epilogue forms
 constexpr int EPI_BF16 = 0;          // out = bf16(scaled accumulator)
@@ -392,6 +395,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tmC,
                     const __grid_constant__ CUtensorMap tmD,
                     const GemmArgs args) {
+  const bool clock_cta = blockIdx.x == 0 && threadIdx.x == 0;
+  const long long clk_start = clock_cta ? clock64() : 0;
+  const unsigned long long ns_start = clock_cta ? globaltimer() : 0ull;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -953,6 +959,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  "r"(TMEM_COLS)
                  : "memory");
   }
+  if (clock_cta) {
+    g_clock_sample[0] = static_cast<unsigned long long>(clock64() - clk_start);
+    g_clock_sample[1] = globaltimer() - ns_start;
+  }
 }
 
 // ------------------------------------------------------------------ host side
@@ -1279,6 +1289,10 @@ cudaError_t launch_wait_selftest(unsigned long long* out, int arrive, unsigned l
                                  cudaStream_t s) {
   wait_selftest_kernel<<<1, 64, 0, s>>>(out, arrive, limit_ns);
   return cudaGetLastError();
+}
+
+cudaError_t gemm_clock_sample(unsigned long long out[2]) {
+  return cudaMemcpyFromSymbol(out, g_clock_sample, 2 * sizeof(unsigned long long));
 }
 
 cudaError_t gemm_take_status(unsigned int* status) {

@@ -67,6 +67,9 @@ cudaError_t launch_gemm_swiglu_bwd(uint16_t* d_gu, float* stats, const uint16_t*
                                    cudaStream_t s);
 // Reads and clears the GEMM kernels' device status word of the current device.
 cudaError_t gemm_take_status(unsigned int* status);
+// SM clock cycles and nanoseconds that the first CTA of the most recent GEMM
+// launch on the current device spent from its start to its end.
+cudaError_t gemm_clock_sample(unsigned long long out[2]);
 // Failure-path self-test of the GEMMs' bounded barrier wait (one CTA, two
 // waits; out[4] as qffn_selftest_bounded_wait documents).
 cudaError_t launch_wait_selftest(unsigned long long* out, int arrive, unsigned long long limit_ns,
