@@ -32,12 +32,15 @@
 //               accumulator barriers to both CTAs at once (multicast).
 //   warps 2..5  epilogue (both CTAs): tcgen05.ld of the fp32 accumulator
 //               (one TMEM lane quarter per warp, one output row per thread,
-//               8 columns per step in a rolled loop), scaling, bf16 rounding,
-//               SwiGLU, abs-max, 16-byte stores (h of the SwiGLU form:
-//               TMA stores of 32 x 64 boxes from a swizzled staging
-//               buffer, two per warp in flight); the
-//               accumulator is handed back to the leader's MMA thread by a
-//               remote mbarrier arrive.
+//               8 columns per step in a rolled loop; the SwiGLU forward
+//               forms at K <= 2048 take 16 per step, the next load in
+//               flight), scaling, bf16 rounding, SwiGLU, abs-max; outputs
+//               leave by TMA stores of 32 x 64 boxes from a swizzled
+//               staging buffer, two per warp in flight (the E4M3 form
+//               stores its codes directly); the accumulator is handed back
+//               to the leader's MMA thread by a remote mbarrier arrive.
+// The first CTA records its SM cycles and nanoseconds from start to end
+// (gemm_clock_sample), from which the launch's mean SM clock follows.
 // Operands are K-major (K contiguous, "TN") by default.  The bf16 form also
 // reads A and / or W MN-major (the M or N index contiguous, i.e. the
 // transposed matrix as it lies in memory): the TMA box is then 128 bytes of
