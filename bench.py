@@ -33,6 +33,7 @@ if ROOT not in sys.path:
 from ffn_inputs import DECODE, PREFILL, decode_inputs, prefill_inputs  # noqa: E402
 
 PREFILL_CFG = PREFILL["llama3-8b"]
+DECODE_LAYERS = 32      # decoder layers of Llama-3-8B: one decode token runs 32 FFNs
 DECODE_CFG = DECODE["llama3-8b-decode"]
 METRIC = "FP8 SwiGLU-FFN fwd TFLOP/s (8B shape, 16k tok)"
 DECODE_METRIC = "M=1 decode FFN HBM GB/s"
@@ -663,17 +664,19 @@ def bench_decode(q, torch, device, iters, dist, peaks):
     cfg = DECODE_CFG
     C, H = cfg.C, cfg.H
     di = decode_inputs(cfg)
-    copies = max(2, -(-2 * L2_BYTES // cfg.weight_bytes) + 1)   # rotate so the weights never sit in L2
-    sets = []
-    for _ in range(copies):
-        s = {}
-        for k, rows, cols in (("w_gate", H, C), ("w_up", H, C), ("w_down", C, H)):
-            wb = to_dev(di[k], torch, device)
-            codes = torch.empty(rows, cols, dtype=torch.uint8, device=device)
-            sc = torch.empty(rows, dtype=torch.float32, device=device)
-            q.qffn_quantize_rows(codes, sc, wb, rows, cols)
-            s[k] = (codes, sc)
-        sets.append(s)
+    # One decode token through the model's FFN layers: a copy of the weights per
+    # layer (32 layers x 176 MB; at least enough copies that no call finds its
+    # weights in L2), the records built once on the GPU and cloned.
+    copies = max(DECODE_LAYERS, -(-2 * L2_BYTES // cfg.weight_bytes) + 1)
+    first = {}
+    for k, rows, cols in (("w_gate", H, C), ("w_up", H, C), ("w_down", C, H)):
+        wb = to_dev(di[k], torch, device)
+        codes = torch.empty(rows, cols, dtype=torch.uint8, device=device)
+        sc = torch.empty(rows, dtype=torch.float32, device=device)
+        q.qffn_quantize_rows(codes, sc, wb, rows, cols)
+        first[k] = (codes, sc)
+        del wb
+    sets = [first] + [{k: (c.clone(), sc.clone()) for k, (c, sc) in first.items()} for _ in range(copies - 1)]
     x = to_dev(di["x"], torch, device)
     out = torch.empty(C, dtype=torch.int16, device=device)
     ws = torch.zeros(q.qffn_decode_workspace_size(C, H), dtype=torch.uint8, device=device)
@@ -686,15 +689,16 @@ def bench_decode(q, torch, device, iters, dist, peaks):
         q.qffn_decode_forward_ex(out, x, *s["w_gate"], *s["w_up"], *s["w_down"], C, H, ws, flags,
                                  stream=stream)
 
-    def graph_us(flags):
+    def graph_us(flags, calls=None):
+        calls = calls or copies
         for i in range(6):
             call(sets[i % copies], flags)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
-            for s in sets:
+            for s in sets[:calls]:
                 call(s, flags)
-        reps = max(1, iters // copies)
+        reps = max(2, -(-iters // calls))
         for _ in range(3):
             graph.replay()
         torch.cuda.synchronize()
@@ -707,11 +711,12 @@ def bench_decode(q, torch, device, iters, dist, peaks):
                 graph.replay()
             t1.record(stream)
         torch.cuda.synchronize()
-        return max_over_ranks(dist, t0.elapsed_time(t1)) * 1e3 / (reps * copies), reps * copies
+        return max_over_ranks(dist, t0.elapsed_time(t1)) * 1e3 / (reps * calls), reps * calls
 
     stable = q.QFFN_DECODE_WEIGHTS_STABLE
     us_graph, n_calls = graph_us(stable)
     us_graph_default, _ = graph_us(0)
+    us_graph3, _ = graph_us(stable, 3)     # a graph of 3 calls replayed (graph launch every 3 calls)
 
     def eager_us(flags):
         e_calls = max(1, iters // copies) * copies
@@ -766,8 +771,10 @@ def bench_decode(q, torch, device, iters, dist, peaks):
     return {
         "metric": DECODE_METRIC, "unit": "GB/s", "value": gbs, "us_per_call": us_graph,
         "bytes_per_call": cfg.weight_bytes, "calls": n_calls, "graph": True,
-        "form": "qffn_decode_forward_ex with QFFN_DECODE_WEIGHTS_STABLE (weights built before the "
-                "timed region), a graph of one call per weight copy, replayed",
+        "form": f"qffn_decode_forward_ex with QFFN_DECODE_WEIGHTS_STABLE (weights built before the "
+                f"timed region): one token through {copies} FFN layers, each with its own weight copy, "
+                f"captured as one CUDA graph of {copies} calls and replayed",
+        "graph_of_3_us_per_call": us_graph3,
         "default_form_us_per_call": us_graph_default,
         "default_form_gbs": cfg.weight_bytes / (us_graph_default * 1e-6) / 1e9,
         "weight_copies_rotated": copies,
