@@ -795,10 +795,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint8_t* qrow = static_cast<uint8_t*>(args.out) + hoff;
         if constexpr (WIDE) {
           // Sixteen columns of g and u per step, two steps per turn of a rolled
-          // loop: the epilogue's code stays small, so it does not crowd the
-          // producer's and the MMA issuer's loops out of the instruction cache
-          // of the SM sub-partitions it shares with them (measured: 2.4% fewer
-          // cycles per GEMM than a fully unrolled 32-column step).  One warp per
+          // loop (the launcher picks this form for K <= 2048, where the
+          // epilogue and not the MMAs sets the tile rate; at longer K the
+          // eight-column loop below measured faster).  One warp per
           // sub-partition runs this loop, so its rate is set by the
           // instruction-level parallelism of a step: sixteen columns give
           // sixteen independent SwiGLU chains, their multiplications paired in
@@ -806,9 +805,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // before this step's arithmetic.
           uint32_t gq[2][16], uq[2][16];
           tmem_ld16x2_issue(tbase, tbase + uint32_t(up_off), gq[0], uq[0]);
-  #pragma unroll 1
+#pragma unroll 1
           for (int c00 = 0; c00 < hcols; c00 += 32) {
-  #pragma unroll
+#pragma unroll
             for (int st = 0; st < 2; ++st) {
               const int c0 = c00 + 16 * st;
               tmem_wait_ld16(gq[st], uq[st]);          // this step's columns have landed
@@ -828,14 +827,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
               }
               uint32_t p[8];
-  #pragma unroll
+#pragma unroll
               for (int j = 0; j < 8; ++j) {
                 p[j] = swiglu_pair(gq[st][2 * j], gq[st][2 * j + 1], uq[st][2 * j], uq[st][2 * j + 1], scale2);
                 if (EPI == EPI_SWIGLU && row_ok) amax2 = bf16x2_absmax(amax2, p[j]);
               }
               if (EPI == EPI_SWIGLU) {
                 const int chunk = (c0 & 63) >> 3;      // even: this step fills chunks chunk, chunk + 1
-  #pragma unroll
+#pragma unroll
                 for (int k = 0; k < 2; ++k)
                   *reinterpret_cast<uint4*>(sbox + lane * 128 + (((chunk + k) ^ (lane & 7)) << 4)) =
                       make_uint4(p[4 * k], p[4 * k + 1], p[4 * k + 2], p[4 * k + 3]);
@@ -853,7 +852,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               if (EPI == EPI_SWIGLU_E4M3 && row_ok) {
                 uint32_t c[4];
-  #pragma unroll
+#pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   const uint16_t lo = qzero ? uint16_t(0)
                                             : f32x2_to_e4m3x2(bf16_lo(p[2 * j]) * qinv, bf16_hi(p[2 * j]) * qinv);
