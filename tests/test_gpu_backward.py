@@ -255,3 +255,58 @@ def test_ffn_backward_8b_shape_sampled(q):
     want = oracle.fp8_gemm_scaled(np.ascontiguousarray(gq_c.T), gs, np.ascontiguousarray(yq[:, ii].T), sy)
     got = bf(g["dw1"])[np.ix_(oi, ii)]
     _check_gemm(got, want, gq_c.T, gs, yq[:, ii].T, sy, max_mismatch=2e-2)
+
+
+@pytest.mark.parametrize("acc", [False, True])
+def test_ffn_backward_graph_capture_equals_eager(q, acc):
+    """qffn_ffn_backward captured in a CUDA graph (its memsets and launches become graph
+    nodes) and replayed twice gives the eager call's bits: the gradients, the stats
+    words and the workspace's dh and d_gate_up."""
+    N, C, H = 208, 384, 256
+    dout, yq, sy, hq, sh, w1q, w1s, w2q, w2s = _backward_inputs(N, C, H, 23)
+    amax = oracle.absmax(dout)
+    dw_init = (random_bf16((2 * H, C), seed=31, std=1e-3), random_bf16((C, H), seed=32, std=1e-3))
+    sc = torch.tensor([sy, sh, w1s, w2s], dtype=torch.float32, device="cuda")
+    d_dout, d_yq, d_hq, d_w1, d_w2 = dev(dout), dev(yq), dev(hq), dev(w1q), dev(w2q)
+    ws_bytes = q.qffn_ffn_backward_workspace_size(N, C, H)
+    off = q.qffn_ffn_backward_workspace_offsets(N, C, H)
+
+    def buffers():
+        return dict(d_ln2=empty_bf16(N, C), dw1=dev(dw_init[0]), dw2=dev(dw_init[1]),
+                    st=torch.tensor([amax, -1.0, -1.0, -1.0], dtype=torch.float32, device="cuda"),
+                    ws=torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda"))
+
+    def run(b, stream=None):
+        q.qffn_ffn_backward(b["d_ln2"], b["dw1"], b["dw2"], b["st"][0:2], b["st"][2:4], d_dout, d_yq, sc[0:1],
+                            d_hq, sc[1:2], d_w1, sc[2:3], d_w2, sc[3:4], N, C, H, acc, b["ws"], stream=stream)
+
+    def snap(b):
+        out = {k: host(b[k]).copy() for k in ("d_ln2", "dw1", "dw2", "st")}
+        out["dh"] = host(b["ws"][off[0]:off[0] + N * H * 2]).copy()
+        out["dgu"] = host(b["ws"][off[1]:off[1] + N * 2 * H * 2]).copy()
+        return out
+
+    eager = buffers()
+    run(eager)
+    q.qffn_check_status()
+    sync()
+    want = snap(eager)
+    b = buffers()
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        run(b, stream=stream)
+    for _ in range(2):
+        # the accumulating form adds into dW: start each replay from the same contents
+        b["dw1"].copy_(dev(dw_init[0]))
+        b["dw2"].copy_(dev(dw_init[1]))
+        b["st"].copy_(torch.tensor([amax, -1.0, -1.0, -1.0]))
+        b["d_ln2"].fill_(-7)
+        b["ws"].zero_()
+        graph.replay()
+        sync()
+        got = snap(b)
+        for k in want:
+            assert np.array_equal(got[k], want[k]), k
+    q.qffn_check_status()

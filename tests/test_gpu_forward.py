@@ -272,3 +272,66 @@ def test_forward_llama3_8b_sampled(q):
     sampled rows stage by stage and end to end."""
     cfg = PREFILL["llama3-8b"]
     check_sampled(q, cfg, _sample_rows(cfg.N, 57))
+
+
+@pytest.mark.parametrize("B,T,C,H", [(2, 32, 256, 768), (3, 43, 256, 384), (1, 300, 2176, 384)])
+def test_forward_graph_capture_equals_eager(q, B, T, C, H):
+    """qffn_forward and qffn_forward_recompute captured in a CUDA graph (their
+    programmatic dependent launches and the abs-max memset become graph nodes) and
+    replayed twice give the eager call's bits in every output and workspace tap.
+    The shapes take both SwiGLU epilogue steps (K <= 2048 and K > 2048)."""
+    cfg = PrefillConfig("graph", B=B, T=T, C=C, H=H, eps=1e-5, seed=B + T + C)
+    inp = prefill_inputs(cfg)
+    N = cfg.N
+    w1, s1 = _gpu_weight_record(q, inp["w1"])
+    w2, s2 = _gpu_weight_record(q, inp["w2"])
+    res, x, gain = dev(inp["res"]), dev(inp["x"]), dev(inp["gain"])
+    ws_bytes = q.qffn_forward_workspace_size(B, T, C, H)
+
+    def buffers():
+        return dict(res_out=empty_bf16(N, C), out=empty_bf16(N, C),
+                    rstd=torch.empty(N, dtype=torch.float32, device="cuda"),
+                    stats=torch.full((4,), -1.0, dtype=torch.float32, device="cuda"),
+                    ws=torch.full((ws_bytes,), 0xAB, dtype=torch.uint8, device="cuda"))
+
+    def fwd(b, stream=None):
+        q.qffn_forward(b["res_out"], b["out"], b["rstd"], b["stats"][0:2], b["stats"][2:4], res, x, gain,
+                       cfg.eps, w1, s1[1:2], w2, s2[1:2], B, T, C, H, b["ws"], stream=stream)
+
+    def rec(b, stream=None):
+        q.qffn_forward_recompute(b["res_out"], b["out"], b["rstd"], b["stats"][0:2], b["stats"][2:4], res, x,
+                                 gain, cfg.eps, w1, s1[1:2], w2, s2[1:2], B, T, C, H, b["ws"], stream=stream)
+
+    def snap(b):
+        return {k: host(v).copy() for k, v in b.items()}
+
+    eager = buffers()
+    fwd(eager)
+    q.qffn_check_status()
+    sync()
+    want = snap(eager)
+    eager_rec = buffers()
+    eager_rec["stats"].copy_(torch.tensor([want["stats"][0], -1.0, want["stats"][2], -1.0]))
+    rec(eager_rec)
+    q.qffn_check_status()
+    sync()
+    want_rec = snap(eager_rec)
+    for call, ref, given in ((fwd, want, None), (rec, want_rec, want["stats"])):
+        b = buffers()
+        stream = torch.cuda.Stream()
+        stream.wait_stream(torch.cuda.current_stream())
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            call(b, stream=stream)
+        for _ in range(2):
+            b["ws"].fill_(0xAB)              # as before the eager call: the recompute form leaves the h slot
+            for k in ("res_out", "out", "rstd"):
+                b[k].fill_(-7)
+            b["stats"].copy_(torch.tensor([-1.0] * 4) if given is None
+                             else torch.tensor([given[0], -1.0, given[2], -1.0]))
+            graph.replay()
+            sync()
+            got = snap(b)
+            for k in ref:
+                assert np.array_equal(got[k], ref[k]), (call.__name__, k)
+        q.qffn_check_status()
