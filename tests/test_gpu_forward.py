@@ -335,3 +335,50 @@ def test_forward_graph_capture_equals_eager(q, B, T, C, H):
             for k in ref:
                 assert np.array_equal(got[k], ref[k]), (call.__name__, k)
         q.qffn_check_status()
+
+
+def test_forward_two_streams_concurrently(q):
+    """Two forwards with their own inputs, outputs and workspaces enqueued on two
+    streams at once (the kernels may interleave on the device) give the bits each
+    gives alone."""
+    cfgs = [PrefillConfig("concurrent", B=2, T=96, C=512, H=768, eps=1e-5, seed=s) for s in (5, 6)]
+    runs = []
+    for cfg in cfgs:
+        inp = prefill_inputs(cfg)
+        w1, s1 = _gpu_weight_record(q, inp["w1"])
+        w2, s2 = _gpu_weight_record(q, inp["w2"])
+        N, C, H = cfg.N, cfg.C, cfg.H
+        ws_bytes = q.qffn_forward_workspace_size(cfg.B, cfg.T, C, H)
+        args = dict(res=dev(inp["res"]), x=dev(inp["x"]), gain=dev(inp["gain"]), w1=w1, s1=s1, w2=w2, s2=s2)
+
+        def buffers(N=N, C=C, ws_bytes=ws_bytes):
+            return dict(res_out=empty_bf16(N, C), out=empty_bf16(N, C),
+                        rstd=torch.empty(N, dtype=torch.float32, device="cuda"),
+                        stats=torch.full((4,), -1.0, dtype=torch.float32, device="cuda"),
+                        ws=torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda"))
+
+        runs.append((cfg, args, buffers))
+
+    def fwd(cfg, a, b, stream):
+        q.qffn_forward(b["res_out"], b["out"], b["rstd"], b["stats"][0:2], b["stats"][2:4], a["res"], a["x"],
+                       a["gain"], cfg.eps, a["w1"], a["s1"][1:2], a["w2"], a["s2"][1:2], cfg.B, cfg.T, cfg.C,
+                       cfg.H, b["ws"], stream=stream)
+
+    alone = []
+    for cfg, a, buffers in runs:
+        b = buffers()
+        fwd(cfg, a, b, None)
+        sync()
+        alone.append({k: host(v).copy() for k, v in b.items()})
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    bufs = [buffers() for _, _, buffers in runs]
+    for rep in range(3):
+        for (cfg, a, _), b, s in zip(runs, bufs, streams):
+            fwd(cfg, a, b, s)
+    sync()
+    q.qffn_check_status()
+    for want, b in zip(alone, bufs):
+        for k, v in want.items():
+            assert np.array_equal(host(b[k]), v), k
